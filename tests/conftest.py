@@ -1,0 +1,24 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA device (B300, sm_103a)")
+    config.addinivalue_line("markers", "slow: full-size problems (minutes of host time)")
+
+
+@pytest.fixture(scope="session")
+def kd():
+    """The CUDA library binding; skips when no GPU is present."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import top_kl_loss_token_b300 as kd_mod
+    kd_mod.load_library()
+    return kd_mod
