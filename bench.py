@@ -1,0 +1,352 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused chunked top-K KL loss (forward + backward).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config 3] [--chunk 0]
+
+One step is one kd_topk_kl_fwd_bwd call over one batch of synthetic inputs:
+teacher preparation, and per token chunk the logsumexp pass, the gradient tile
+and both gradient GEMMs (every row of the hot path).  The default workload is
+the large-vocabulary long-context case: N = 32,768 tokens, d = 2880,
+V = 201,088, K = 100 teacher entries, T = 1, bf16 h and W.  Throughput is
+tokens/s of the whole job; TFLOP/s counts 6 N d V per step (forward logits,
+grad_h and grad_W products).  Inputs are larger than L2 (W alone is 1.16 GB),
+so no flush is needed between steps.
+
+Under torchrun (N > 1) every rank runs its own token shard of the same size
+(weak scaling, no collective on the data path); the barrier and max-over-ranks
+time use torch.distributed.  `--impl reference` times the fp64 CPU oracle on a
+bounded sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused KL fwd+bwd tokens/s and TFLOP/s (% of B300 bf16 peak); peak GiB"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_name(x) -> str:
+    mask = f", {x.masked_fraction() * 100:.1f}% masked" if x.mask is not None else ""
+    return (f"{x.name}: N={x.N} tokens, d={x.d}, V={x.V}, K={x.K}, T={x.T:g}, "
+            f"{x.dtype} h/W, fp32 teacher top-K{mask}")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_oracle_time(x, rows: int):
+    """Times the fp64 oracle's fwd+bwd on the first `rows` tokens of x."""
+    import oracle
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max([i.get("num_threads", 1) for i in threadpool_info()] or [os.cpu_count()])
+    except Exception:
+        cores = os.cpu_count()
+    h = x.h_f32()[:rows].astype(np.float64)
+    W = x.W_f32().astype(np.float64)
+    m = None if x.mask is None else x.mask[:rows]
+    t0 = time.perf_counter()
+    oracle.fwd_bwd(h, W, x.idx[:rows], x.logit[:rows], m, x.T)
+    dt = time.perf_counter() - t0
+    return dt, cores
+
+
+def run_reference(args, x):
+    """The oracle as the reference arm: each step is a bounded sample of the workload."""
+    rows = args.ref_rows
+    for _ in range(args.warmup):
+        cpu_oracle_time(x, rows)
+    times, cores = [], 1
+    for _ in range(args.steps):
+        dt, cores = cpu_oracle_time(x, rows)
+        times.append(dt)
+    total = sum(times)
+    value = rows * args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_name(x), "sample": f"first {rows} tokens per step"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"fwd+bwd of the first {rows} of {x.N} tokens, per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", type=int, default=3)
+    ap.add_argument("--chunk", type=int, default=0)
+    ap.add_argument("--cpu-rows", type=int, default=512,
+                    help="tokens in the CPU-oracle baseline sample")
+    ap.add_argument("--ref-rows", type=int, default=64,
+                    help="tokens per step of the reference (oracle) arm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
+
+    from top_kl_loss_token_b300 import synth
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        x = synth.make_config(args.config)
+        run_reference(args, x)
+        return
+
+    import torch
+    import torch.distributed as dist
+    import top_kl_loss_token_b300 as kd
+
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local_rank if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    kd.load_library()
+
+    x = synth.make_config(args.config)
+    if world > 1:
+        # each rank's token shard: same sizes, its own seed
+        c = dict(synth.CONFIGS[args.config])
+        c["seed"] = c["seed"] + 1000 * rank
+        x = synth.make_inputs(**c)
+    N, d, V, K = x.N, x.d, x.V, x.K
+    dt_code = kd.KD_BF16 if x.dtype == "bf16" else kd.KD_FP32
+    chunk = args.chunk if args.chunk > 0 else kd.default_chunk(N, d, V, dt_code)
+
+    # host copies (pinned) and resident device inputs
+    if x.dtype == "bf16":
+        h_host = torch.from_numpy(x.h.view(np.int16)).view(torch.bfloat16)
+        W_host = torch.from_numpy(x.W.view(np.int16)).view(torch.bfloat16)
+    else:
+        h_host, W_host = torch.from_numpy(x.h), torch.from_numpy(x.W)
+    idx_host = torch.from_numpy(x.idx)
+    lg_host = torch.from_numpy(x.logit)
+    m_host = None if x.mask is None else torch.from_numpy(x.mask)
+    h_pin, idx_pin, lg_pin = h_host.pin_memory(), idx_host.pin_memory(), lg_host.pin_memory()
+    m_pin = None if m_host is None else m_host.pin_memory()
+    W = W_host.to(dev)
+    h, idx, lg = h_pin.to(dev), idx_pin.to(dev), lg_pin.to(dev)
+    mask = None if m_pin is None else m_pin.to(dev)
+    base_alloc = torch.cuda.memory_allocated(dev)
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    grad_h = torch.empty((N, d), dtype=torch.float32, device=dev)
+    grad_W = torch.empty((V, d), dtype=torch.float32, device=dev)
+    ws_bytes = kd.workspace_bytes(N, d, V, K, chunk, dt_code)
+    torch.cuda.reset_peak_memory_stats(dev)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kd.fwd_bwd(h, W, idx, lg, mask, x.T, chunk, loss=loss, grad_h=grad_h, grad_W=grad_W,
+                   workspace=ws, err_flags=err, stream=stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error flags {int(err.item())}")
+    peak_extra = (torch.cuda.max_memory_allocated(dev) - base_alloc) / 2 ** 30
+
+    # ---------------- timed region: inputs resident in HBM
+    kd.timing_enable(True)
+    kd.timing_collect()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        barrier()
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+    kd.timing_enable(False)
+    kernels = kd.timing_collect()
+    ms = ev0.elapsed_time(ev1)
+    ms_t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms = float(ms_t.item())
+    tokens_total = N * args.steps * world
+    value = tokens_total / (ms / 1000.0)
+    flops_step = 6.0 * N * d * V
+    tflops = flops_step * args.steps * world / (ms / 1000.0) / 1e12 / world  # per GPU
+
+    # ---------------- end to end: H2D of the step's inputs, D2H of the loss
+    loss_host = torch.empty(1, dtype=torch.float32).pin_memory()
+    h2d = h_pin.numel() * h_pin.element_size() + idx_pin.numel() * 4 + lg_pin.numel() * 4
+    if m_pin is not None:
+        h2d += m_pin.numel()
+    e_steps = max(1, min(args.steps, 5))
+    barrier()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        h.copy_(h_pin, non_blocking=True)
+        idx.copy_(idx_pin, non_blocking=True)
+        lg.copy_(lg_pin, non_blocking=True)
+        if m_pin is not None:
+            mask.copy_(m_pin, non_blocking=True)
+        step()
+        loss_host.copy_(loss, non_blocking=True)
+        stream.synchronize()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    e_ms = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(e_ms, op=dist.ReduceOp.MAX)
+    e_value = N * e_steps * world / (float(e_ms.item()) / 1000.0)
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    # ---------------- roofline of the dominant kernel
+    peaks, peaks_src = load_peaks()
+    n_chunks = -(-N // chunk)
+    valid_tokens = N if x.mask is None else int(x.mask.sum())
+    # algorithmic flops per token of each tensor-core kernel
+    per_token = {"pass1_gemm": 2.0 * d * V, "bwd_gemm": 4.0 * d * V}
+    dom = max(kernels.items(), key=lambda kv: kv[1][1])[0] if kernels else None
+    roof = None
+    if dom in per_token:
+        launches, tot_ms = kernels[dom]
+        flops_per_launch = per_token[dom] * valid_tokens * args.steps / launches
+        achieved = flops_per_launch / (tot_ms / launches / 1000.0) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                "peak_source": f"{peaks_src} bf16 sustained (kernel timed inside a long step)",
+                "flops_per_launch": flops_per_launch,
+                "avg_launch_ms": tot_ms / launches}
+    launches_total = sum(v[0] for v in kernels.values())
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        rows = min(args.cpu_rows, N)
+        dtc, cores = cpu_oracle_time(x, rows)
+        cpu = {"value": rows / dtc, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"fp64 oracle fwd+bwd of the first {rows} of {N} tokens ({dtc:.1f} s)"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": x.dtype,
+        "data": "synthetic",
+        "config": {"workload": workload_name(x), "chunk": chunk, "n_chunks": n_chunks,
+                   "l2": "inputs larger than L2 (W alone 1.16 GB), no flush",
+                   "parallelism": f"token shards x{world}" if world > 1 else "1 GPU"},
+        "tflops_per_gpu": tflops,
+        "pct_of_bf16_peak": {"burst": tflops / peaks["bf16_tflops"],
+                             "sustained": tflops / peaks["bf16_tflops_sustained"],
+                             "source": peaks_src},
+        "peak_extra_gib": peak_extra,
+        "workspace_gib": ws_bytes / 2 ** 30,
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": 4},
+        "gpu_launches": launches_total,
+        "kernels": {k: {"launches": v[0], "ms": v[1]} for k, v in kernels.items()},
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

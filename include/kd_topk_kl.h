@@ -1,0 +1,138 @@
+/*
+ * kd_topk_kl.h -- fused chunked top-K KL distillation loss on B300 (sm_103a).
+ *
+ * The operation is the KL-divergence distillation loss of a student against an
+ * offline teacher cache that keeps only the teacher's top K predictions per
+ * position ("Efficient Knowledge Distillation for LLMs: Offline Top-K Logits
+ * and a Fused Chunked KL Loss"; ai2day.live story, section "What did the
+ * researchers change?": the teacher's top 100 predictions per position are
+ * cached once, and the loss is computed over the sequence chunk by chunk, each
+ * chunk calculated and discarded, the backward pass recomputing what it needs).
+ * The loss is computed from the student's final hidden states and LM-head
+ * weight without ever building the N x V student-logit grid (aiphreaks.com
+ * summary, second paragraph; elseif.net summary, third paragraph); extra
+ * device memory is O(chunk * V + N * K).
+ *
+ * Definitions (natural log; T is the temperature shared by teacher and student):
+ *   p_r      = softmax over the K cached entries of (topk_logit_r / T)
+ *   z        = h W^T,   s = z / T,   lse_r = logsumexp over the vocabulary of s_r
+ *   loss     = (1 / N_valid) * sum over valid rows r of
+ *                sum_k p_rk * (log p_rk - (s_{r, idx_rk} - lse_r))
+ *   dL/dz_rv = (softmax(s_r)_v - sum_{k : idx_rk = v} p_rk) / (T * N_valid)
+ *   grad_h   = (dL/dz) W        grad_W = (dL/dz)^T h
+ * There is no T^2 factor.  N_valid counts the valid rows; with N_valid = 0 the
+ * loss and both gradients are 0.
+ *
+ * Layouts (all row-major, contiguous, 16-byte aligned device buffers):
+ *   h          [N, d]   bf16 or fp32 (dtype)          student final hidden states
+ *   W          [V, d]   same dtype as h                LM-head weight (nn.Linear layout)
+ *   topk_idx   [N, K]   int32                          teacher vocabulary indices
+ *   topk_logit [N, K]   fp32                           teacher logits (or log-probs)
+ *   mask       [N]      uint8, 1 = valid, 0 = ignored; NULL means every row valid
+ *   loss       [1]      fp32, written
+ *   grad_h     [N, d]   fp32, overwritten (rows that are not valid are set to 0)
+ *   grad_W     [V, d]   fp32, overwritten
+ * d must be a multiple of 8 (bf16) or 4 (fp32): the rows are read by the tensor
+ * memory accelerator, whose strides are multiples of 16 bytes.
+ *
+ * Row validity and data errors (found on the device, reported through
+ * *dev_err_flags, which the library ORs bits into; the caller zeroes it and
+ * reads it after synchronising the stream):
+ *   KD_FLAG_INDEX_RANGE  an index of a valid row lies outside [0, V): that
+ *                        entry is dropped from the teacher distribution (as if
+ *                        its logit were -inf).
+ *   KD_FLAG_BAD_TEACHER  a valid row whose in-range teacher logits contain NaN
+ *                        or +inf, or no finite value: the row is treated as
+ *                        masked (no loss, zero grad_h row, not in N_valid).
+ *   KD_FLAG_TIMEOUT      a wait inside a kernel gave up after its time limit;
+ *                        the results of that call are not valid.
+ * A -inf teacher logit is legal and gives that entry probability 0.  A
+ * duplicate index within a row adds its probabilities.  Masked rows' data
+ * (h, topk_idx, topk_logit) is never read for a result.
+ *
+ * Ownership and execution: the caller owns every buffer (inputs, outputs and
+ * the workspace).  The library allocates no memory and keeps no per-call state;
+ * every call is stream-ordered and asynchronous on `stream` (0 = the legacy
+ * default stream).  The returned status reports only the synchronous host-side
+ * checks and launch errors.  Two calls may run concurrently only with distinct
+ * workspaces.
+ */
+#ifndef KD_TOPK_KL_H
+#define KD_TOPK_KL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KD_OK = 0,
+  KD_ERR_INVALID_ARG = 1,  /* null pointer, negative size, K < 1, bad T, ... */
+  KD_ERR_UNSUPPORTED = 2,  /* a size this build does not handle (see below)  */
+  KD_ERR_WORKSPACE = 3,    /* workspace NULL or smaller than required        */
+  KD_ERR_CUDA = 4          /* a CUDA call or kernel launch failed            */
+} kd_status;
+
+typedef enum { KD_BF16 = 0, KD_FP32 = 1 } kd_dtype;
+
+#define KD_FLAG_INDEX_RANGE 1u
+#define KD_FLAG_BAD_TEACHER 2u
+#define KD_FLAG_TIMEOUT 4u
+
+/* Largest K accepted (the per-row sort of the teacher entries runs in shared
+ * memory); larger K returns KD_ERR_UNSUPPORTED. */
+#define KD_MAX_K 4096
+
+/*
+ * Bytes of device workspace a call with these sizes needs.  chunk <= 0 asks
+ * for the default chunk (kd_topk_kl_default_chunk).  Returns 0 for invalid
+ * sizes.  The workspace holds, per call: the teacher probabilities and sorted
+ * indices (O(N K)), per-row statistics (O(N)), and one chunk's
+ * vocabulary-wide buffers (O(chunk V)).  It needs no initialisation.
+ */
+size_t kd_topk_kl_workspace_bytes(int64_t N, int64_t d, int64_t V, int32_t K, int64_t chunk,
+                                  kd_dtype dtype);
+
+/* The chunk (in tokens) used when a call passes chunk <= 0. */
+int64_t kd_topk_kl_default_chunk(int64_t N, int64_t d, int64_t V, kd_dtype dtype);
+
+/*
+ * Loss, grad_h and grad_W in one pass over the token chunks.
+ *   chunk      tokens per chunk (the unit whose vocabulary-wide buffers live
+ *              in the workspace); <= 0 picks the default.  The result does not
+ *              depend on it beyond floating-point rounding.
+ *   T          temperature, finite and > 0.
+ *   dev_err_flags  optional device uint32 (see above); NULL keeps the flags in
+ *              the workspace only.
+ * Errors: KD_ERR_INVALID_ARG (a required pointer is NULL; N < 0; d, V or K < 1;
+ * K > KD_MAX_K is KD_ERR_UNSUPPORTED; T not finite or <= 0), KD_ERR_UNSUPPORTED
+ * (d not a multiple of 8 for bf16 / 4 for fp32), KD_ERR_WORKSPACE, KD_ERR_CUDA.
+ * With N = 0, h, topk_idx, topk_logit, mask and grad_h may be NULL; loss and
+ * grad_W are written as 0.
+ */
+kd_status kd_topk_kl_fwd_bwd(const void* h, const void* W, kd_dtype dtype,
+                             const int32_t* topk_idx, const float* topk_logit,
+                             const uint8_t* mask, int64_t N, int64_t d, int64_t V, int32_t K,
+                             float T, int64_t chunk, float* loss, float* grad_h, float* grad_W,
+                             void* workspace, size_t ws_bytes, uint32_t* dev_err_flags,
+                             cudaStream_t stream);
+
+/* The loss alone (same definition and arguments, no gradient outputs). */
+kd_status kd_topk_kl_fwd(const void* h, const void* W, kd_dtype dtype, const int32_t* topk_idx,
+                         const float* topk_logit, const uint8_t* mask, int64_t N, int64_t d,
+                         int64_t V, int32_t K, float T, int64_t chunk, float* loss,
+                         void* workspace, size_t ws_bytes, uint32_t* dev_err_flags,
+                         cudaStream_t stream);
+
+/* A static, human-readable name for a status code. */
+const char* kd_status_string(kd_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KD_TOPK_KL_H */

@@ -1,0 +1,98 @@
+/*
+ * kd_topk_kl_steps.h -- step-level entry points of the kd_topk_kl library.
+ *
+ * These expose pieces of the fused top-K KL loss (see kd_topk_kl.h) so that a
+ * test can check each one on its own:
+ *   - the layout of the workspace, so the per-row intermediate results a call
+ *     leaves there (the student log-partition lse_r and the per-row loss terms
+ *     of "Efficient Knowledge Distillation for LLMs: Offline Top-K Logits and a
+ *     Fused Chunked KL Loss", ai2day.live story, "What did the researchers
+ *     change?") can be compared with a reference;
+ *   - the tensor-core matrix product the three contractions of that loss use
+ *     (z = h W^T, grad_h = G W, grad_W = G^T h), as a plain GEMM.
+ * Same conventions as kd_topk_kl.h: caller-owned device buffers, nothing
+ * allocated, stream-ordered, host-side status only.
+ */
+#ifndef KD_TOPK_KL_STEPS_H
+#define KD_TOPK_KL_STEPS_H
+
+#include "kd_topk_kl.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * Where a call with these sizes keeps its intermediates inside the workspace
+ * (byte offsets from the workspace base, each 256-byte aligned).  Valid after
+ * a kd_topk_kl_fwd_bwd / kd_topk_kl_fwd call has completed on its stream:
+ *   ctrl:      uint32 error flags at +0, int32 N_valid at +4, double loss sum at +8
+ *   rows:      int32 [N]  original row of the i-th valid row (i < N_valid)
+ *   lse:       fp32  [N]  lse_i of the i-th valid row (natural log, of s = z/T)
+ *   loss_rows: fp32  [N]  loss term of the i-th valid row (before the 1/N_valid)
+ * The other regions are scratch space whose contents are not specified.
+ */
+typedef struct {
+  int64_t chunk;      /* resolved chunk, in tokens                              */
+  int64_t chunk_pad;  /* rows of each per-chunk buffer (multiple of 128)        */
+  int64_t n_pb;       /* 128-column vocabulary blocks, ceil(V / 128)           */
+  int64_t ld_g;       /* row stride, in elements, of the per-chunk vocab buffer */
+  size_t off_ctrl;
+  size_t off_row_ok;
+  size_t off_rows;
+  size_t off_idx_sorted;
+  size_t off_p_sorted;
+  size_t off_plogp;
+  size_t off_psum;
+  size_t off_lse;
+  size_t off_loss_rows;
+  size_t off_part_m;
+  size_t off_part_l;
+  size_t off_part_ps;
+  size_t off_boff;
+  size_t off_hc;
+  size_t off_g;
+  size_t off_sched;
+  size_t total;
+} kd_workspace_layout;
+
+kd_status kd_topk_kl_workspace_layout(int64_t N, int64_t d, int64_t V, int32_t K, int64_t chunk,
+                                      kd_dtype dtype, kd_workspace_layout* out);
+
+/*
+ * D[M, N] (fp32, row-major, leading dimension N) = sum_k A(m, k) * B(n, k) on
+ * the tcgen05 tensor cores, bf16 inputs, fp32 accumulation; D += ... when
+ * accumulate != 0.
+ *   a_mn_major = 0: A is [M, K] row-major (K contiguous); 1: A is [K, M] (M contiguous)
+ *   b_mn_major = 0: B is [N, K] row-major (K contiguous); 1: B is [K, N] (N contiguous)
+ * The contiguous dimension of each operand must be a multiple of 8 elements
+ * (16-byte rows).  counter is one device uint32 of scratch that the call
+ * resets and uses to hand out tiles.  Errors as in kd_topk_kl.h.
+ */
+kd_status kd_umma_gemm_bf16(const void* A, const void* B, float* D, int64_t M, int64_t N,
+                            int64_t K, int a_mn_major, int b_mn_major, int accumulate,
+                            uint32_t* counter, uint32_t* dev_err_flags, cudaStream_t stream);
+
+/*
+ * Kernel timing (instrumentation; the write-ups define no counterpart).  While
+ * enabled, the library brackets each of its kernel launches with a pair of
+ * CUDA events recorded on the launching stream.  kd_timing_collect waits for
+ * those events, returns one entry per kernel kind (launch count and summed
+ * device time), and clears the record.  Host-side state shared by all calls
+ * of the process; not thread-safe; off by default.
+ */
+typedef struct {
+  char name[32];      /* kernel kind, e.g. "pass1_gemm", "bwd_gemm"          */
+  int64_t launches;   /* launches recorded since the last collect             */
+  double total_ms;    /* summed CUDA-event time of those launches             */
+} kd_timing_entry;
+
+kd_status kd_timing_enable(int on);
+/* Writes up to max_entries entries; *n_entries receives the number of kinds. */
+kd_status kd_timing_collect(kd_timing_entry* out, int32_t max_entries, int32_t* n_entries);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KD_TOPK_KL_STEPS_H */

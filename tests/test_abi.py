@@ -1,0 +1,103 @@
+"""Host-side checks of the C ABI: the library loads, exports every function the
+headers declare, plans workspaces, and rejects bad arguments before touching
+a GPU (these run without one)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import top_kl_loss_token_b300 as kd
+from top_kl_loss_token_b300 import build as kd_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(kd.LIB_PATH):
+        kd_build.build()
+    return kd.load_library()
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(kd_[a-z0-9_]+)\s*\(",
+                             text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    decl = declared_functions()
+    assert decl == set(kd.EXPORTS), decl ^ set(kd.EXPORTS)
+    for name in decl:
+        assert hasattr(lib, name), name
+
+
+def test_workspace_plan_is_linear_in_chunk_not_in_n_times_v(lib):
+    # Extra memory is O(chunk * V + N * K): quadrupling N at a fixed chunk adds
+    # only O(N K) bytes, not O(N V).
+    V, d, K, c = 201088, 2880, 100, 8192
+    a = kd.workspace_bytes(32768, d, V, K, c)
+    b = kd.workspace_bytes(131072, d, V, K, c)
+    assert b - a < (131072 - 32768) * (8 * K + 64)
+    dense = 131072 * V * 2
+    assert b < dense / 10
+    lay = kd.workspace_layout(32768, d, V, K, c)
+    assert lay.chunk == c and lay.chunk_pad == c and lay.n_pb == (V + 127) // 128
+    offs = [getattr(lay, f[0]) for f in kd.WorkspaceLayout._fields_ if f[0].startswith("off_")]
+    assert all(o % 256 == 0 for o in offs)
+    assert offs == sorted(offs) and lay.total >= offs[-1]
+
+
+def test_default_chunk_splits_evenly(lib):
+    assert kd.default_chunk(32768, 2880, 201088) == 8192
+    c = kd.default_chunk(131072, 2880, 201088)
+    assert c % 128 == 0 and c * 2 * ((201088 + 255) // 256 * 256) <= 4 << 30
+    assert kd.default_chunk(64, 64, 512, kd.KD_FP32) == 128
+
+
+def call_fwd_bwd(lib, **kw):
+    args = dict(h=16, W=16, dtype=kd.KD_BF16, idx=16, logit=16, mask=None, N=8, d=16, V=32, K=4,
+                T=1.0, chunk=0, loss=16, gh=16, gW=16, ws=16, ws_bytes=1 << 40, err=None, stream=None)
+    args.update(kw)
+    return lib.kd_topk_kl_fwd_bwd(args["h"], args["W"], args["dtype"], args["idx"], args["logit"],
+                                  args["mask"], args["N"], args["d"], args["V"], args["K"],
+                                  args["T"], args["chunk"], args["loss"], args["gh"], args["gW"],
+                                  args["ws"], args["ws_bytes"], args["err"], args["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(W=None), 1), (dict(loss=None), 1), (dict(h=None), 1), (dict(gh=None), 1),
+    (dict(N=-1), 1), (dict(d=0), 1), (dict(V=0), 1), (dict(K=0), 1),
+    (dict(K=kd.KD_MAX_K + 1), 2), (dict(T=0.0), 1), (dict(T=float("nan")), 1),
+    (dict(T=float("inf")), 1), (dict(T=-1.0), 1), (dict(d=12), 2), (dict(dtype=7), 1),
+    (dict(dtype=kd.KD_FP32, d=6), 2), (dict(ws=None), 3), (dict(ws_bytes=100), 3),
+    (dict(W=24), 1), (dict(ws=40), 3),
+])
+def test_host_side_argument_errors(lib, kw, status):
+    assert call_fwd_bwd(lib, **kw) == status
+
+
+def test_status_strings(lib):
+    for s in range(5):
+        assert lib.kd_status_string(s)
+    assert kd.status_string(3) == "workspace missing or too small"
+
+
+def test_umma_gemm_argument_errors(lib):
+    f = lib.kd_umma_gemm_bf16
+    assert f(16, 16, 16, 0, 8, 8, 0, 0, 0, 16, 16, None) == 1
+    assert f(16, 16, 16, 8, 8, 12, 0, 0, 0, 16, 16, None) == 2   # K-major A with K % 8 != 0
+    assert f(16, 16, 16, 12, 8, 8, 1, 0, 0, 16, 16, None) == 2   # MN-major A with M % 8 != 0
+    assert f(None, 16, 16, 8, 8, 8, 0, 0, 0, 16, 16, None) == 1
+
+
+def test_build_flags_target_sm103a():
+    assert "arch=compute_103a,code=sm_103a" in kd_build.ARCH

@@ -1,1 +1,261 @@
-"""Fused chunked top-K KL distillation loss for B300 (sm_103a)."""
+"""Fused chunked top-K KL distillation loss for B300 (sm_103a).
+
+Python binding of the C ABI in include/kd_topk_kl.h and
+include/kd_topk_kl_steps.h.  It only marshals arguments: torch provides the
+device memory and the stream, every step runs in the CUDA kernels of
+libkd_topk_kl.so.  There is no other implementation behind these functions;
+if the library is missing they raise.
+
+The loss is the KL divergence of a student against an offline teacher cache
+of the top K (index, logit) pairs per position ("Efficient Knowledge
+Distillation for LLMs: Offline Top-K Logits and a Fused Chunked KL Loss",
+ai2day.live story, "What did the researchers change?"), computed chunk by
+chunk over the tokens without materialising the N x V logit grid.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG_DIR, "libkd_topk_kl.so")
+
+KD_BF16 = 0
+KD_FP32 = 1
+KD_FLAG_INDEX_RANGE = 1
+KD_FLAG_BAD_TEACHER = 2
+KD_FLAG_TIMEOUT = 4
+KD_MAX_K = 4096
+
+STATUS = {0: "KD_OK", 1: "KD_ERR_INVALID_ARG", 2: "KD_ERR_UNSUPPORTED", 3: "KD_ERR_WORKSPACE",
+          4: "KD_ERR_CUDA"}
+
+# Every symbol the headers declare.
+EXPORTS = ["kd_topk_kl_workspace_bytes", "kd_topk_kl_default_chunk", "kd_topk_kl_fwd_bwd",
+           "kd_topk_kl_fwd", "kd_status_string", "kd_topk_kl_workspace_layout",
+           "kd_umma_gemm_bf16", "kd_timing_enable", "kd_timing_collect"]
+
+_LIB = None
+
+
+class KDError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+        self.status = status
+
+
+class WorkspaceLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in ("chunk", "chunk_pad", "n_pb", "ld_g")] + [
+        (n, ctypes.c_size_t) for n in (
+            "off_ctrl", "off_row_ok", "off_rows", "off_idx_sorted", "off_p_sorted", "off_plogp",
+            "off_psum", "off_lse", "off_loss_rows", "off_part_m", "off_part_l", "off_part_ps",
+            "off_boff", "off_hc", "off_g", "off_sched", "total")]
+
+
+class TimingEntry(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 32), ("launches", ctypes.c_int64),
+                ("total_ms", ctypes.c_double)]
+
+
+def load_library(path: str = LIB_PATH):
+    """Loads libkd_topk_kl.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with `python -m top_kl_loss_token_b300.build`")
+    lib = ctypes.CDLL(path)
+    i64, i32, f32, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_float, ctypes.c_void_p
+    sz = ctypes.c_size_t
+    lib.kd_topk_kl_workspace_bytes.argtypes = [i64, i64, i64, i32, i64, ctypes.c_int]
+    lib.kd_topk_kl_workspace_bytes.restype = sz
+    lib.kd_topk_kl_default_chunk.argtypes = [i64, i64, i64, ctypes.c_int]
+    lib.kd_topk_kl_default_chunk.restype = i64
+    lib.kd_topk_kl_workspace_layout.argtypes = [i64, i64, i64, i32, i64, ctypes.c_int,
+                                                ctypes.POINTER(WorkspaceLayout)]
+    lib.kd_topk_kl_workspace_layout.restype = ctypes.c_int
+    lib.kd_topk_kl_fwd_bwd.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, i64, i64, i64, i32, f32,
+                                       i64, vp, vp, vp, vp, sz, vp, vp]
+    lib.kd_topk_kl_fwd_bwd.restype = ctypes.c_int
+    lib.kd_topk_kl_fwd.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, i64, i64, i64, i32, f32, i64,
+                                   vp, vp, sz, vp, vp]
+    lib.kd_topk_kl_fwd.restype = ctypes.c_int
+    lib.kd_status_string.argtypes = [ctypes.c_int]
+    lib.kd_status_string.restype = ctypes.c_char_p
+    lib.kd_umma_gemm_bf16.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_int, vp, vp, vp]
+    lib.kd_umma_gemm_bf16.restype = ctypes.c_int
+    lib.kd_timing_enable.argtypes = [ctypes.c_int]
+    lib.kd_timing_enable.restype = ctypes.c_int
+    lib.kd_timing_collect.argtypes = [ctypes.POINTER(TimingEntry), i32, ctypes.POINTER(i32)]
+    lib.kd_timing_collect.restype = ctypes.c_int
+    _LIB = lib
+    return lib
+
+
+def _check(st: int, where: str):
+    if st != 0:
+        raise KDError(st, where)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return KD_BF16
+    if t.dtype == torch.float32:
+        return KD_FP32
+    raise TypeError(f"h and W must be bfloat16 or float32, got {t.dtype}")
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream) -> int:
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def workspace_bytes(N: int, d: int, V: int, K: int, chunk: int = 0, dtype: int = KD_BF16) -> int:
+    n = load_library().kd_topk_kl_workspace_bytes(N, d, V, K, chunk, dtype)
+    if n == 0:
+        raise KDError(1, "kd_topk_kl_workspace_bytes")
+    return int(n)
+
+
+def default_chunk(N: int, d: int, V: int, dtype: int = KD_BF16) -> int:
+    return int(load_library().kd_topk_kl_default_chunk(N, d, V, dtype))
+
+
+def workspace_layout(N: int, d: int, V: int, K: int, chunk: int = 0,
+                     dtype: int = KD_BF16) -> WorkspaceLayout:
+    lay = WorkspaceLayout()
+    _check(load_library().kd_topk_kl_workspace_layout(N, d, V, K, chunk, dtype, ctypes.byref(lay)),
+           "kd_topk_kl_workspace_layout")
+    return lay
+
+
+def _validate(h, W, idx, logit, mask):
+    import torch
+    for name, t in (("h", h), ("W", W), ("topk_idx", idx), ("topk_logit", logit)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if h.dtype != W.dtype:
+        raise TypeError("h and W must have the same dtype")
+    if idx.dtype != torch.int32 or logit.dtype != torch.float32:
+        raise TypeError("topk_idx must be int32 and topk_logit float32")
+    if mask is not None and (mask.dtype != torch.uint8 or not mask.is_cuda
+                             or not mask.is_contiguous()):
+        raise TypeError("mask must be a contiguous uint8 CUDA tensor")
+    N, d = h.shape
+    V, d2 = W.shape
+    if d2 != d or idx.shape != logit.shape or idx.shape[0] != N:
+        raise ValueError("shape mismatch")
+    if mask is not None and mask.shape != (N,):
+        raise ValueError("mask must have shape [N]")
+    return N, d, V, idx.shape[1]
+
+
+def allocate_workspace(N, d, V, K, chunk=0, dtype=KD_BF16, device=None):
+    import torch
+    n = workspace_bytes(N, d, V, K, chunk, dtype)
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def kd_topk_kl_fwd_bwd(h, W, topk_idx, topk_logit, mask=None, T: float = 1.0, chunk: int = 0,
+                       loss=None, grad_h=None, grad_W=None, workspace=None, err_flags=None,
+                       stream=None):
+    """Loss, grad_h and grad_W of the top-K KL loss (see include/kd_topk_kl.h).
+
+    Returns (loss [1] fp32, grad_h [N, d] fp32, grad_W [V, d] fp32, workspace).
+    Asynchronous on the current (or given) stream."""
+    import torch
+    N, d, V, K = _validate(h, W, topk_idx, topk_logit, mask)
+    dt = _dtype_code(h)
+    dev = h.device
+    if loss is None:
+        loss = torch.empty(1, dtype=torch.float32, device=dev)
+    if grad_h is None:
+        grad_h = torch.empty((N, d), dtype=torch.float32, device=dev)
+    if grad_W is None:
+        grad_W = torch.empty((V, d), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = allocate_workspace(N, d, V, K, chunk, dt, dev)
+    st = load_library().kd_topk_kl_fwd_bwd(
+        _ptr(h), _ptr(W), dt, _ptr(topk_idx), _ptr(topk_logit), _ptr(mask), N, d, V, K,
+        float(T), int(chunk), _ptr(loss), _ptr(grad_h), _ptr(grad_W), _ptr(workspace),
+        workspace.numel(), _ptr(err_flags), _stream_handle(stream))
+    _check(st, "kd_topk_kl_fwd_bwd")
+    return loss, grad_h, grad_W, workspace
+
+
+def kd_topk_kl_fwd(h, W, topk_idx, topk_logit, mask=None, T: float = 1.0, chunk: int = 0,
+                   loss=None, workspace=None, err_flags=None, stream=None):
+    """The loss alone.  Returns (loss [1] fp32, workspace)."""
+    import torch
+    N, d, V, K = _validate(h, W, topk_idx, topk_logit, mask)
+    dt = _dtype_code(h)
+    if loss is None:
+        loss = torch.empty(1, dtype=torch.float32, device=h.device)
+    if workspace is None:
+        workspace = allocate_workspace(N, d, V, K, chunk, dt, h.device)
+    st = load_library().kd_topk_kl_fwd(
+        _ptr(h), _ptr(W), dt, _ptr(topk_idx), _ptr(topk_logit), _ptr(mask), N, d, V, K,
+        float(T), int(chunk), _ptr(loss), _ptr(workspace), workspace.numel(), _ptr(err_flags),
+        _stream_handle(stream))
+    _check(st, "kd_topk_kl_fwd")
+    return loss, workspace
+
+
+def kd_umma_gemm_bf16(A, B, M: int, N: int, K: int, a_mn_major: bool, b_mn_major: bool,
+                      out=None, accumulate: bool = False, err_flags=None, stream=None):
+    """D[M, N] (+)= A(m, k) B(n, k) on the tensor cores (see kd_topk_kl_steps.h)."""
+    import torch
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    counter = torch.empty(1, dtype=torch.int32, device=A.device)
+    if err_flags is None:
+        err_flags = torch.zeros(1, dtype=torch.int32, device=A.device)
+    st = load_library().kd_umma_gemm_bf16(_ptr(A), _ptr(B), _ptr(out), M, N, K, int(a_mn_major),
+                                          int(b_mn_major), int(accumulate), _ptr(counter),
+                                          _ptr(err_flags), _stream_handle(stream))
+    _check(st, "kd_umma_gemm_bf16")
+    return out, err_flags
+
+
+def kd_timing_enable(on: bool = True):
+    """Bracket every kernel launch of the library with CUDA events (see
+    kd_topk_kl_steps.h)."""
+    _check(load_library().kd_timing_enable(int(on)), "kd_timing_enable")
+
+
+def kd_timing_collect():
+    """Waits for the recorded events; returns {kernel kind: (launches, total ms)}
+    and clears the record."""
+    arr = (TimingEntry * 32)()
+    n = ctypes.c_int32(0)
+    _check(load_library().kd_timing_collect(arr, 32, ctypes.byref(n)), "kd_timing_collect")
+    return {arr[i].name.decode(): (int(arr[i].launches), float(arr[i].total_ms))
+            for i in range(min(n.value, 32))}
+
+
+def status_string(st: int) -> str:
+    return load_library().kd_status_string(st).decode()
+
+
+def workspace_view(workspace, lay: WorkspaceLayout, name: str, count: int, dtype):
+    """A typed view of one documented region of a workspace (see
+    kd_topk_kl_workspace_layout): 'ctrl', 'rows', 'lse' or 'loss_rows'."""
+    import torch
+    off = getattr(lay, "off_" + name)
+    nbytes = count * torch.empty(0, dtype=dtype).element_size()
+    return workspace[off: off + nbytes].view(dtype)
+
+
+# Short names.
+fwd_bwd = kd_topk_kl_fwd_bwd
+fwd = kd_topk_kl_fwd
+timing_enable = kd_timing_enable
+timing_collect = kd_timing_collect

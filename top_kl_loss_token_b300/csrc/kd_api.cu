@@ -1,0 +1,570 @@
+// kd_api.cu -- host side of the kd_topk_kl C ABI: argument checks, the
+// workspace plan, tensor-map encoding and the chunk loop that launches the
+// kernels of the fused top-K KL loss on the caller's stream.
+//
+// The chunk loop is the method of "Efficient Knowledge Distillation for LLMs:
+// Offline Top-K Logits and a Fused Chunked KL Loss" (ai2day.live story, "What
+// did the researchers change?"): the sequence is sliced into chunks, each
+// chunk's vocabulary-wide buffers are computed, used and overwritten by the
+// next chunk, so device memory grows as O(chunk * V + N * K), never O(N * V).
+#include <math.h>
+#include <string.h>
+
+#include <mutex>
+#include <vector>
+
+#include "kd_internal.h"
+
+namespace kd {
+
+namespace {
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ------------------------------------------------------------- kernel timing
+enum Kind {
+  kTeacherPrep,
+  kCompact,
+  kZeroRows,
+  kGatherRows,
+  kBucketOffsets,
+  kPass1Gemm,
+  kLseCombine,
+  kGradTile,
+  kBwdGemm,
+  kFinalize,
+  kSimtPass1,
+  kSimtGemm,
+  kNumKinds
+};
+const char* const kKindNames[kNumKinds] = {
+    "teacher_prep", "compact",    "zero_invalid_rows", "gather_rows", "bucket_offsets",
+    "pass1_gemm",   "lse_combine", "grad_tile",        "bwd_gemm",    "finalize",
+    "simt_pass1",   "simt_gemm"};
+
+struct TimingRec {
+  int kind;
+  cudaEvent_t a, b;
+};
+bool g_timing_on = false;
+std::vector<TimingRec> g_recs;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t pooled_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Brackets one launch with events when timing is on.
+struct TimedLaunch {
+  int kind;
+  cudaStream_t s;
+  cudaEvent_t a = nullptr;
+  TimedLaunch(int k, cudaStream_t st) : kind(k), s(st) {
+    if (g_timing_on) {
+      a = pooled_event();
+      if (a != nullptr) cudaEventRecord(a, s);
+    }
+  }
+  ~TimedLaunch() {
+    if (a == nullptr) return;
+    cudaEvent_t b = pooled_event();
+    if (b == nullptr) return;
+    cudaEventRecord(b, s);
+    g_recs.push_back(TimingRec{kind, a, b});
+  }
+};
+
+}  // namespace
+
+bool encode_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                      uint64_t ld_elems, uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {ld_elems * 2};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int64_t default_chunk(int64_t N, int64_t d, int64_t V, kd_dtype dtype) {
+  (void)d;
+  const int64_t elem = dtype == KD_BF16 ? 2 : 4;
+  const int64_t ldg = round_up(V, kBN);
+  // Keep the per-chunk vocabulary buffer near 4 GiB: a few chunks per call
+  // amortise the grad_W read-modify-write while the extra memory stays small
+  // next to HBM.
+  // The chunks are then made equal (multiples of 128 rows) so the last one
+  // is not a small remainder.
+  const int64_t budget = int64_t(4) << 30;
+  int64_t cmax = budget / (ldg * elem);
+  cmax = cmax / kBM * kBM;
+  if (cmax < kBM) cmax = kBM;
+  if (cmax > 16384) cmax = 16384;
+  const int64_t n = N < 1 ? 1 : N;
+  const int64_t pieces = ceil_div(n, cmax);
+  return round_up(ceil_div(n, pieces), kBM);
+}
+
+kd_status make_plan(int64_t N, int64_t d, int64_t V, int32_t K, int64_t chunk, kd_dtype dtype,
+                    Plan* p) {
+  if (dtype != KD_BF16 && dtype != KD_FP32) return KD_ERR_INVALID_ARG;
+  if (N < 0 || d < 1 || V < 1 || K < 1) return KD_ERR_INVALID_ARG;
+  if (K > KD_MAX_K) return KD_ERR_UNSUPPORTED;
+  if (N >= (int64_t(1) << 31) || V >= (int64_t(1) << 31) - 1024 || d >= (int64_t(1) << 24))
+    return KD_ERR_UNSUPPORTED;
+  if ((dtype == KD_BF16 && d % 8 != 0) || (dtype == KD_FP32 && d % 4 != 0))
+    return KD_ERR_UNSUPPORTED;
+  Plan& P = *p;
+  P.N = N;
+  P.d = d;
+  P.V = V;
+  P.K = K;
+  P.dtype = dtype;
+  P.elem = dtype == KD_BF16 ? 2 : 4;
+  int64_t c = chunk > 0 ? chunk : default_chunk(N, d, V, dtype);
+  if (N > 0 && c > N) c = N;
+  if (c < 1) c = 1;
+  if (c >= (int64_t(1) << 30)) return KD_ERR_UNSUPPORTED;
+  P.chunk = c;
+  P.cpad = round_up(c, kBM);
+  P.n_pb = ceil_div(V, kPB);
+  P.ldg = round_up(V, kBN);
+  P.n_chunks = N > 0 ? ceil_div(N, c) : 0;
+  kd_workspace_layout& L = P.lay;
+  memset(&L, 0, sizeof(L));
+  L.chunk = P.chunk;
+  L.chunk_pad = P.cpad;
+  L.n_pb = P.n_pb;
+  L.ld_g = P.ldg;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align256(o + bytes);
+    return at;
+  };
+  const size_t n = static_cast<size_t>(N);
+  const size_t nk = n * static_cast<size_t>(K);
+  const size_t part = static_cast<size_t>(P.n_pb) * static_cast<size_t>(P.cpad);
+  L.off_ctrl = take(256);
+  L.off_row_ok = take(4 * n);
+  L.off_rows = take(4 * n);
+  L.off_idx_sorted = take(4 * nk);
+  L.off_p_sorted = take(4 * nk);
+  L.off_plogp = take(4 * n);
+  L.off_psum = take(4 * n);
+  L.off_lse = take(4 * n);
+  L.off_loss_rows = take(4 * n);
+  L.off_part_m = take(4 * part);
+  L.off_part_l = take(4 * part);
+  L.off_part_ps = take(4 * part);
+  L.off_boff = take(2 * (static_cast<size_t>(P.n_pb) + 1) * static_cast<size_t>(P.cpad));
+  L.off_hc = take(static_cast<size_t>(P.cpad) * static_cast<size_t>(d) * P.elem);
+  L.off_g = take(static_cast<size_t>(P.cpad) * static_cast<size_t>(P.ldg) * P.elem);
+  L.off_sched = take(256);
+  L.total = o;
+  return KD_OK;
+}
+
+namespace {
+
+struct Views {
+  Ctrl* ctrl;
+  int32_t* row_ok;
+  int32_t* rows;
+  int32_t* idx_sorted;
+  float* p_sorted;
+  float* plogp;
+  float* psum;
+  float* lse;
+  float* loss_rows;
+  float* part_m;
+  float* part_l;
+  float* part_ps;
+  uint16_t* boff;
+  void* hc;
+  void* g;
+  uint32_t* sched;
+};
+
+Views views(const Plan& P, void* ws) {
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  const kd_workspace_layout& L = P.lay;
+  Views v;
+  v.ctrl = reinterpret_cast<Ctrl*>(b + L.off_ctrl);
+  v.row_ok = reinterpret_cast<int32_t*>(b + L.off_row_ok);
+  v.rows = reinterpret_cast<int32_t*>(b + L.off_rows);
+  v.idx_sorted = reinterpret_cast<int32_t*>(b + L.off_idx_sorted);
+  v.p_sorted = reinterpret_cast<float*>(b + L.off_p_sorted);
+  v.plogp = reinterpret_cast<float*>(b + L.off_plogp);
+  v.psum = reinterpret_cast<float*>(b + L.off_psum);
+  v.lse = reinterpret_cast<float*>(b + L.off_lse);
+  v.loss_rows = reinterpret_cast<float*>(b + L.off_loss_rows);
+  v.part_m = reinterpret_cast<float*>(b + L.off_part_m);
+  v.part_l = reinterpret_cast<float*>(b + L.off_part_l);
+  v.part_ps = reinterpret_cast<float*>(b + L.off_part_ps);
+  v.boff = reinterpret_cast<uint16_t*>(b + L.off_boff);
+  v.hc = b + L.off_hc;
+  v.g = b + L.off_g;
+  v.sched = reinterpret_cast<uint32_t*>(b + L.off_sched);
+  return v;
+}
+
+#define KD_CUDA(x)                            \
+  do {                                        \
+    if ((x) != cudaSuccess) return KD_ERR_CUDA; \
+  } while (0)
+
+// A kernel launch (through its launch function) with optional timing.
+#define KD_LAUNCH(kind, x)              \
+  do {                                  \
+    TimedLaunch timed_launch_(kind, stream); \
+    KD_CUDA(x);                         \
+  } while (0)
+
+kd_status run(const void* h, const void* W, kd_dtype dtype, const int32_t* topk_idx,
+              const float* topk_logit, const uint8_t* mask, int64_t N, int64_t d, int64_t V,
+              int32_t K, float T, int64_t chunk, float* loss, float* grad_h, float* grad_W,
+              bool want_grads, void* workspace, size_t ws_bytes, uint32_t* dev_err_flags,
+              cudaStream_t stream) {
+  Plan P;
+  kd_status st = make_plan(N, d, V, K, chunk, dtype, &P);
+  if (st != KD_OK) return st;
+  if (!(T > 0.f) || !isfinite(T)) return KD_ERR_INVALID_ARG;
+  if (W == nullptr || loss == nullptr) return KD_ERR_INVALID_ARG;
+  if (want_grads && grad_W == nullptr) return KD_ERR_INVALID_ARG;
+  if (N > 0 && (h == nullptr || topk_idx == nullptr || topk_logit == nullptr))
+    return KD_ERR_INVALID_ARG;
+  if (want_grads && N > 0 && grad_h == nullptr) return KD_ERR_INVALID_ARG;
+  if (!aligned16(W) || (N > 0 && !aligned16(h))) return KD_ERR_INVALID_ARG;
+  if (workspace == nullptr || ws_bytes < P.lay.total) return KD_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return KD_ERR_WORKSPACE;
+  const int sms = num_sms();
+  if (sms <= 0) return KD_ERR_CUDA;
+  if (dtype == KD_BF16 && encode_fn() == nullptr) return KD_ERR_CUDA;
+
+  const Views v = views(P, workspace);
+  uint32_t* err = dev_err_flags != nullptr ? dev_err_flags : &v.ctrl->err;
+  KD_CUDA(cudaMemsetAsync(v.ctrl, 0, sizeof(Ctrl), stream));
+  if (N == 0) {
+    KD_CUDA(cudaMemsetAsync(loss, 0, sizeof(float), stream));
+    if (want_grads)
+      KD_CUDA(cudaMemsetAsync(grad_W, 0, static_cast<size_t>(V) * d * sizeof(float), stream));
+    return KD_OK;
+  }
+  const float k2 = 1.4426950408889634f / T;
+
+  KD_LAUNCH(kTeacherPrep, launch_teacher_prep(topk_idx, topk_logit, mask, N, K, V, T, v.row_ok, v.idx_sorted,
+                              v.p_sorted, v.plogp, v.psum, err, stream));
+  KD_LAUNCH(kCompact, launch_compact(v.row_ok, N, v.rows, v.ctrl, stream));
+  if (want_grads) KD_LAUNCH(kZeroRows, launch_zero_invalid_rows(v.row_ok, N, d, grad_h, stream));
+
+  for (int64_t j = 0; j < P.n_chunks; ++j) {
+    ChunkArgs a;
+    a.row0 = j * P.chunk;
+    a.chunk = static_cast<int>(P.chunk);
+    a.cpad = P.cpad;
+    a.n_valid = &v.ctrl->n_valid;
+    a.rows = v.rows;
+    a.idx_sorted = v.idx_sorted;
+    a.p_sorted = v.p_sorted;
+    a.K = K;
+    a.V = static_cast<int>(V);
+    a.n_pb = static_cast<int>(P.n_pb);
+    a.ldg = P.ldg;
+    a.boff = v.boff;
+    a.part_m = v.part_m;
+    a.part_l = v.part_l;
+    a.part_ps = v.part_ps;
+
+    KD_LAUNCH(kGatherRows, launch_gather_rows(h, P.elem, d, a, v.hc, stream));
+    KD_LAUNCH(kBucketOffsets, launch_bucket_offsets(a, stream));
+    if (dtype == KD_BF16) {
+      Pass1Args p1;
+      p1.hc = v.hc;
+      p1.W = W;
+      p1.d = d;
+      p1.k2 = k2;
+      p1.u = static_cast<uint16_t*>(v.g);
+      p1.counter = v.sched;
+      p1.err = err;
+      p1.num_sms = sms;
+      KD_LAUNCH(kPass1Gemm, launch_tc_pass1(p1, a, stream));
+    } else {
+      KD_LAUNCH(kSimtPass1, launch_simt_pass1(static_cast<const float*>(v.hc), static_cast<const float*>(W), d,
+                                a, k2, static_cast<float*>(v.g), stream));
+    }
+    KD_LAUNCH(kLseCombine, launch_lse(a, v.plogp, v.psum, T, v.lse, v.loss_rows, stream));
+    if (!want_grads) continue;
+    KD_LAUNCH(kGradTile, launch_grad_tile(a, v.g, P.elem, T, stream));
+    if (dtype == KD_BF16) {
+      TcGemmArgs g;
+      memset(&g, 0, sizeof(g));
+      TcProblem& gh = g.pr[0];  // grad_h rows of the chunk = G_c W
+      gh.A = v.g;
+      gh.a_mn = 0;
+      gh.a_inner = V;
+      gh.a_outer = P.cpad;
+      gh.lda = P.ldg;
+      gh.B = W;
+      gh.b_mn = 1;
+      gh.b_inner = d;
+      gh.b_outer = V;
+      gh.ldb = d;
+      gh.M = P.chunk;
+      gh.N = d;
+      gh.K = V;
+      gh.out = grad_h;
+      gh.ldo = d;
+      gh.row_map = v.rows;
+      gh.row_map_off = a.row0;
+      gh.accumulate = 0;
+      gh.count_mode = 1;
+      TcProblem& gw = g.pr[1];  // grad_W (+)= G_c^T h_c
+      gw.A = v.g;
+      gw.a_mn = 1;
+      gw.a_inner = V;
+      gw.a_outer = P.cpad;
+      gw.lda = P.ldg;
+      gw.B = v.hc;
+      gw.b_mn = 1;
+      gw.b_inner = d;
+      gw.b_outer = P.cpad;
+      gw.ldb = d;
+      gw.M = V;
+      gw.N = d;
+      gw.K = P.chunk;
+      gw.out = grad_W;
+      gw.ldo = d;
+      gw.row_map = nullptr;
+      gw.accumulate = j > 0 ? 1 : 0;
+      gw.count_mode = 2;
+      g.nprob = 2;
+      g.n_valid = a.n_valid;
+      g.row0 = a.row0;
+      g.chunk = a.chunk;
+      g.counter = v.sched + 1;
+      g.err = err;
+      g.num_sms = sms;
+      KD_LAUNCH(kBwdGemm, launch_tc_gemm(g, stream));
+    } else {
+      const float* G = static_cast<const float*>(v.g);
+      SimtGemm gh;
+      memset(&gh, 0, sizeof(gh));
+      gh.A = G;
+      gh.sam = P.ldg;
+      gh.sak = 1;
+      gh.B = static_cast<const float*>(W);
+      gh.sbk = d;
+      gh.sbn = 1;
+      gh.C = grad_h;
+      gh.ldc = d;
+      gh.M_cap = P.chunk;
+      gh.N = d;
+      gh.Kfix = V;
+      gh.m_from_count = 1;
+      gh.row_map = v.rows;
+      gh.row_map_off = a.row0;
+      gh.n_valid = a.n_valid;
+      gh.row0 = a.row0;
+      KD_LAUNCH(kSimtGemm, launch_simt_gemm(gh, stream));
+      SimtGemm gw;
+      memset(&gw, 0, sizeof(gw));
+      gw.A = G;
+      gw.sam = 1;
+      gw.sak = P.ldg;
+      gw.B = static_cast<const float*>(v.hc);
+      gw.sbk = d;
+      gw.sbn = 1;
+      gw.C = grad_W;
+      gw.ldc = d;
+      gw.M_cap = V;
+      gw.N = d;
+      gw.Kfix = P.chunk;
+      gw.k_from_count = 1;
+      gw.accumulate = j > 0 ? 1 : 0;
+      gw.n_valid = a.n_valid;
+      gw.row0 = a.row0;
+      KD_LAUNCH(kSimtGemm, launch_simt_gemm(gw, stream));
+    }
+  }
+  KD_LAUNCH(kFinalize, launch_finalize(v.loss_rows, v.ctrl, loss, stream));
+  return KD_OK;
+}
+
+}  // namespace
+}  // namespace kd
+
+extern "C" {
+
+size_t kd_topk_kl_workspace_bytes(int64_t N, int64_t d, int64_t V, int32_t K, int64_t chunk,
+                                  kd_dtype dtype) {
+  kd::Plan p;
+  if (kd::make_plan(N, d, V, K, chunk, dtype, &p) != KD_OK) return 0;
+  return p.lay.total;
+}
+
+int64_t kd_topk_kl_default_chunk(int64_t N, int64_t d, int64_t V, kd_dtype dtype) {
+  return kd::default_chunk(N, d, V, dtype);
+}
+
+kd_status kd_topk_kl_workspace_layout(int64_t N, int64_t d, int64_t V, int32_t K, int64_t chunk,
+                                      kd_dtype dtype, kd_workspace_layout* out) {
+  if (out == nullptr) return KD_ERR_INVALID_ARG;
+  kd::Plan p;
+  const kd_status st = kd::make_plan(N, d, V, K, chunk, dtype, &p);
+  if (st != KD_OK) return st;
+  *out = p.lay;
+  return KD_OK;
+}
+
+kd_status kd_topk_kl_fwd_bwd(const void* h, const void* W, kd_dtype dtype,
+                             const int32_t* topk_idx, const float* topk_logit,
+                             const uint8_t* mask, int64_t N, int64_t d, int64_t V, int32_t K,
+                             float T, int64_t chunk, float* loss, float* grad_h, float* grad_W,
+                             void* workspace, size_t ws_bytes, uint32_t* dev_err_flags,
+                             cudaStream_t stream) {
+  return kd::run(h, W, dtype, topk_idx, topk_logit, mask, N, d, V, K, T, chunk, loss, grad_h,
+                 grad_W, true, workspace, ws_bytes, dev_err_flags, stream);
+}
+
+kd_status kd_topk_kl_fwd(const void* h, const void* W, kd_dtype dtype, const int32_t* topk_idx,
+                         const float* topk_logit, const uint8_t* mask, int64_t N, int64_t d,
+                         int64_t V, int32_t K, float T, int64_t chunk, float* loss,
+                         void* workspace, size_t ws_bytes, uint32_t* dev_err_flags,
+                         cudaStream_t stream) {
+  return kd::run(h, W, dtype, topk_idx, topk_logit, mask, N, d, V, K, T, chunk, loss, nullptr,
+                 nullptr, false, workspace, ws_bytes, dev_err_flags, stream);
+}
+
+kd_status kd_umma_gemm_bf16(const void* A, const void* B, float* D, int64_t M, int64_t N,
+                            int64_t K, int a_mn_major, int b_mn_major, int accumulate,
+                            uint32_t* counter, uint32_t* dev_err_flags, cudaStream_t stream) {
+  if (A == nullptr || B == nullptr || D == nullptr || counter == nullptr ||
+      dev_err_flags == nullptr)
+    return KD_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1) return KD_ERR_INVALID_ARG;
+  if (M >= (int64_t(1) << 30) || N >= (int64_t(1) << 30) || K >= (int64_t(1) << 30))
+    return KD_ERR_UNSUPPORTED;
+  const int64_t a_inner = a_mn_major ? M : K, a_outer = a_mn_major ? K : M;
+  const int64_t b_inner = b_mn_major ? N : K, b_outer = b_mn_major ? K : N;
+  if (a_inner % 8 != 0 || b_inner % 8 != 0) return KD_ERR_UNSUPPORTED;
+  if (!kd::aligned16(A) || !kd::aligned16(B)) return KD_ERR_INVALID_ARG;
+  if (kd::encode_fn() == nullptr) return KD_ERR_CUDA;
+  const int sms = kd::num_sms();
+  if (sms <= 0) return KD_ERR_CUDA;
+  kd::TcGemmArgs g;
+  memset(&g, 0, sizeof(g));
+  kd::TcProblem& p = g.pr[0];
+  p.A = A;
+  p.a_mn = a_mn_major ? 1 : 0;
+  p.a_inner = a_inner;
+  p.a_outer = a_outer;
+  p.lda = a_inner;
+  p.B = B;
+  p.b_mn = b_mn_major ? 1 : 0;
+  p.b_inner = b_inner;
+  p.b_outer = b_outer;
+  p.ldb = b_inner;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.out = D;
+  p.ldo = N;
+  p.accumulate = accumulate ? 1 : 0;
+  g.nprob = 1;
+  g.chunk = static_cast<int>(M);
+  g.counter = counter;
+  g.err = dev_err_flags;
+  g.num_sms = sms;
+  return kd::launch_tc_gemm(g, stream) == cudaSuccess ? KD_OK : KD_ERR_CUDA;
+}
+
+kd_status kd_timing_enable(int on) {
+  kd::g_timing_on = on != 0;
+  return KD_OK;
+}
+
+kd_status kd_timing_collect(kd_timing_entry* out, int32_t max_entries, int32_t* n_entries) {
+  int64_t launches[kd::kNumKinds] = {0};
+  double ms[kd::kNumKinds] = {0.0};
+  kd_status st = KD_OK;
+  for (const kd::TimingRec& r : kd::g_recs) {
+    float t = 0.f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess)
+      st = KD_ERR_CUDA;
+    launches[r.kind] += 1;
+    ms[r.kind] += t;
+    kd::g_event_pool.push_back(r.a);
+    kd::g_event_pool.push_back(r.b);
+  }
+  kd::g_recs.clear();
+  int32_t n = 0;
+  for (int k = 0; k < kd::kNumKinds; ++k) {
+    if (launches[k] == 0) continue;
+    if (out != nullptr && n < max_entries) {
+      memset(out[n].name, 0, sizeof(out[n].name));
+      strncpy(out[n].name, kd::kKindNames[k], sizeof(out[n].name) - 1);
+      out[n].launches = launches[k];
+      out[n].total_ms = ms[k];
+    }
+    ++n;
+  }
+  if (n_entries != nullptr) *n_entries = n;
+  return st;
+}
+
+const char* kd_status_string(kd_status s) {
+  switch (s) {
+    case KD_OK:
+      return "ok";
+    case KD_ERR_INVALID_ARG:
+      return "invalid argument";
+    case KD_ERR_UNSUPPORTED:
+      return "unsupported size";
+    case KD_ERR_WORKSPACE:
+      return "workspace missing or too small";
+    case KD_ERR_CUDA:
+      return "CUDA error";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

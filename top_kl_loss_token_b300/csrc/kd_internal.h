@@ -1,0 +1,161 @@
+// kd_internal.h -- shared between the host driver and the kernel files of
+// the kd_topk_kl library: tile constants, the workspace plan, and the launch
+// functions of every kernel.  Not part of the public interface.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kd_topk_kl.h"
+#include "kd_topk_kl_steps.h"
+
+namespace kd {
+
+// Tensor-core tiles: one CTA owns a 128 x 256 fp32 accumulator in TMEM (two of
+// them, double-buffered) and streams 64-deep K blocks of both operands
+// through a 4-stage shared-memory ring.
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+// The logsumexp statistics are kept per 128-column block of the vocabulary.
+constexpr int kPB = 128;
+// A sorted-index slot that holds no entry (dropped, or padding).
+constexpr int kNoIndex = 0x7fffffff;
+
+__host__ __device__ constexpr int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+__host__ __device__ constexpr int64_t ceil_div(int64_t x, int64_t m) { return (x + m - 1) / m; }
+
+// Workspace plan for one call; all offsets 256-byte aligned.
+struct Plan {
+  int64_t N, d, V, K, chunk, cpad, n_pb, ldg, n_chunks;
+  kd_dtype dtype;
+  size_t elem;  // bytes per h/W/G element
+  kd_workspace_layout lay;
+};
+
+// Fills `p` and returns KD_OK, or an error for invalid sizes.
+kd_status make_plan(int64_t N, int64_t d, int64_t V, int32_t K, int64_t chunk, kd_dtype dtype,
+                    Plan* p);
+int64_t default_chunk(int64_t N, int64_t d, int64_t V, kd_dtype dtype);
+
+// Control words at the start of the workspace.
+struct Ctrl {
+  uint32_t err;     // error flags when the caller passes none
+  int32_t n_valid;  // number of valid rows
+  double loss_sum;  // sum of the per-row loss terms
+};
+
+// Per-chunk pointers into the workspace that the row kernels use.
+struct ChunkArgs {
+  int64_t row0;          // first compacted row of this chunk
+  int chunk;             // capacity of the chunk, in rows
+  int64_t cpad;          // row stride of the per-chunk statistic arrays
+  const int32_t* n_valid;
+  const int32_t* rows;   // compacted row -> original row
+  const int32_t* idx_sorted;
+  const float* p_sorted;
+  int K;
+  int V;
+  int n_pb;
+  int64_t ldg;
+  uint16_t* boff;        // [n_pb + 1][cpad] first sorted entry of each 128-column block
+  float* part_m;         // [n_pb][cpad]  block max of z * log2(e) / T (then alpha)
+  float* part_l;         // [n_pb][cpad]  block sum of 2^(s2 - m2)
+  float* part_ps;        // [n_pb][cpad]  block sum of p_k * s2_k over teacher entries
+};
+
+// ----------------------------------------------------------- row kernels
+cudaError_t launch_teacher_prep(const int32_t* idx, const float* logit, const uint8_t* mask,
+                                int64_t N, int K, int64_t V, float T, int32_t* row_ok,
+                                int32_t* idx_sorted, float* p_sorted, float* plogp, float* psum,
+                                uint32_t* err, cudaStream_t s);
+cudaError_t launch_compact(const int32_t* row_ok, int64_t N, int32_t* rows, Ctrl* ctrl,
+                           cudaStream_t s);
+cudaError_t launch_gather_rows(const void* h, size_t elem, int64_t d, const ChunkArgs& a,
+                               void* hc, cudaStream_t s);
+cudaError_t launch_bucket_offsets(const ChunkArgs& a, cudaStream_t s);
+cudaError_t launch_lse(const ChunkArgs& a, const float* plogp, const float* psum, float T,
+                       float* lse, float* loss_rows, cudaStream_t s);
+cudaError_t launch_grad_tile(const ChunkArgs& a, void* g, size_t elem, float T, cudaStream_t s);
+cudaError_t launch_finalize(const float* loss_rows, Ctrl* ctrl, float* loss, cudaStream_t s);
+cudaError_t launch_zero_invalid_rows(const int32_t* row_ok, int64_t N, int64_t d, float* grad_h,
+                                     cudaStream_t s);
+
+// ----------------------------------------------------------- fp32 CUDA-core path
+cudaError_t launch_simt_pass1(const float* hc, const float* W, int64_t d, const ChunkArgs& a,
+                              float k2, float* u, cudaStream_t s);
+// C(m, n) (+)= sum_k A(m, k) B(k, n); A(m, k) = A[m * sam + k * sak], B(k, n) = B[k * sbk + n * sbn].
+// M rows of C may be limited on the device to count = clamp(*n_valid - row0, 0, M_cap);
+// with k_from_count the K extent is that count instead of Kfix.
+struct SimtGemm {
+  const float* A;
+  int64_t sam, sak;
+  const float* B;
+  int64_t sbk, sbn;
+  float* C;
+  int64_t ldc;
+  int64_t M_cap, N, Kfix;
+  int m_from_count, k_from_count;
+  const int32_t* row_map;  // C row = row_map[row_map_off + m] when non-null
+  int64_t row_map_off;
+  int accumulate;          // C += instead of C =; with K = 0 and accumulate = 0, C = 0
+  const int32_t* n_valid;
+  int64_t row0;
+};
+cudaError_t launch_simt_gemm(const SimtGemm& g, cudaStream_t s);
+
+// ----------------------------------------------------------- tensor-core path
+// Encodes a 2-D bf16 tensor map (inner dimension contiguous) with 128-byte
+// swizzle and the given box.  Returns false if the driver rejects it.
+bool encode_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                      uint64_t ld_elems, uint32_t box_inner, uint32_t box_outer);
+
+struct Pass1Args {
+  const void* hc;  // [cpad, d] bf16
+  const void* W;   // [V, d] bf16
+  int64_t d;
+  float k2;        // log2(e) / T
+  uint16_t* u;     // [cpad, ldg] bf16, written
+  uint32_t* counter;
+  uint32_t* err;
+  int num_sms;
+};
+cudaError_t launch_tc_pass1(const Pass1Args& p, const ChunkArgs& a, cudaStream_t s);
+
+// One or two GEMM problems in one persistent launch, fp32 results stored (or
+// accumulated) row by row: out[row(m), n] (+)= sum_k A(m, k) B(n, k).
+struct TcProblem {
+  // Stored operands (bf16, row-major with the given leading dimension).  A
+  // K-major operand is stored [rows, K] (inner = K); an MN-major one is
+  // stored [K, rows] (inner = M or N).
+  const void* A;
+  int a_mn;
+  int64_t a_inner, a_outer, lda;
+  const void* B;
+  int b_mn;
+  int64_t b_inner, b_outer, ldb;
+  int64_t M, N, K;   // output rows, output columns, reduction length (capacities)
+  float* out;
+  int64_t ldo;
+  const int32_t* row_map;  // output row = row_map[row_map_off + m] when non-null
+  int64_t row_map_off;
+  int accumulate;
+  // With count_mode != 0 an extent is clamped on the device to
+  // count = clamp(*n_valid - row0, 0, chunk):  1: M = count,  2: K = count.
+  int count_mode;
+};
+struct TcGemmArgs {
+  TcProblem pr[2];
+  int nprob;
+  const int32_t* n_valid;
+  int64_t row0;
+  int chunk;
+  uint32_t* counter;
+  uint32_t* err;
+  int num_sms;
+};
+cudaError_t launch_tc_gemm(const TcGemmArgs& g, cudaStream_t s);
+
+}  // namespace kd

@@ -1,0 +1,738 @@
+// kd_rowops.cu -- the row-wise kernels of the fused top-K KL loss and its
+// fp32 CUDA-core path.
+//
+// "Efficient Knowledge Distillation for LLMs: Offline Top-K Logits and a Fused
+// Chunked KL Loss" keeps only the teacher's top K (index, logit) pairs per
+// position (ai2day.live story, "What did the researchers change?") and drops
+// the rest of the teacher distribution (elseif.net summary, third paragraph).
+// These kernels turn that cache into renormalised probabilities, combine the
+// per-block logsumexp statistics of the student logits into the per-token
+// loss, form the gradient of the loss with respect to the logits one chunk at
+// a time, and reduce the loss.  Every exponential is taken in base 2:
+// s2 = z * log2(e) / T, so softmax(z / T) = 2^(s2 - lse2).
+#include <math.h>
+#include <stdint.h>
+
+#include "kd_internal.h"
+#include "kd_ptx.cuh"
+
+namespace kd {
+namespace {
+
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ int chunk_count(const int32_t* n_valid, int64_t row0, int chunk) {
+  const long long c = static_cast<long long>(*n_valid) - row0;
+  return c < 0 ? 0 : (c > chunk ? chunk : static_cast<int>(c));
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ int warp_or(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v |= __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// ------------------------------------------------------------- teacher prep
+//
+// One block per token row r:
+//   valid row     mask[r] != 0 (or no mask) and a usable teacher row;
+//   drop          entries whose index is outside [0, V) (flag INDEX_RANGE);
+//   bad row       a NaN or +inf among the in-range logits, or no finite one
+//                 (flag BAD_TEACHER; the row is then treated as masked);
+//   p_k           = 2^(t2_k - max t2) / sum, t2 = logit * log2(e) / T
+//                 (renormalised over the kept entries, -inf -> 0);
+//   plogp         = sum_k p_k ln p_k,  psum = sum_k p_k;
+//   sorted list   the kept (index, p) pairs in increasing index order,
+//                 padded with (kNoIndex, 0) up to K.
+constexpr int kPrepThreads = 128;
+
+__global__ void __launch_bounds__(kPrepThreads) teacher_prep_kernel(
+    const int32_t* __restrict__ idx, const float* __restrict__ logit,
+    const uint8_t* __restrict__ mask, int K, int64_t V, float k2, int P2,
+    int32_t* __restrict__ row_ok, int32_t* __restrict__ idx_sorted,
+    float* __restrict__ p_sorted, float* __restrict__ plogp, float* __restrict__ psum,
+    uint32_t* __restrict__ err) {
+  extern __shared__ uint8_t sm[];
+  int32_t* skey = reinterpret_cast<int32_t*>(sm);
+  float* sval = reinterpret_cast<float*>(skey + P2);
+  __shared__ float red_f[kPrepThreads / 32];
+  __shared__ int red_i[kPrepThreads / 32];
+
+  const int64_t r = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  if (mask != nullptr && mask[r] == 0) {
+    if (tid == 0) row_ok[r] = 0;
+    return;
+  }
+  const int32_t* ri = idx + r * K;
+  const float* rl = logit + r * K;
+
+  // Pass A: drop out-of-range entries, find bad rows, max of t2.
+  int bits = 0;  // 1: out of range seen, 2: NaN / +inf seen, 4: finite seen
+  float mx = -INFINITY;
+  for (int k = tid; k < P2; k += kPrepThreads) {
+    int key = kNoIndex;
+    float t2 = -INFINITY;
+    if (k < K) {
+      const int32_t v = ri[k];
+      const float l = rl[k];
+      if (v < 0 || static_cast<int64_t>(v) >= V) {
+        bits |= 1;
+      } else {
+        key = v;
+        if (isnan(l) || l == INFINITY) bits |= 2;
+        if (isfinite(l)) bits |= 4;
+        t2 = l * k2;
+        mx = fmaxf(mx, t2);
+      }
+    }
+    skey[k] = key;
+    sval[k] = t2;
+  }
+  bits = warp_or(bits);
+  mx = warp_max(mx);
+  if (lane == 0) {
+    red_i[wid] = bits;
+    red_f[wid] = mx;
+  }
+  __syncthreads();
+  bits = 0;
+  mx = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kPrepThreads / 32; ++w) {
+    bits |= red_i[w];
+    mx = fmaxf(mx, red_f[w]);
+  }
+  __syncthreads();
+  const bool bad = (bits & 2) || !(bits & 4);
+  if (tid == 0) {
+    uint32_t f = 0;
+    if (bits & 1) f |= KD_FLAG_INDEX_RANGE;
+    if (bad) f |= KD_FLAG_BAD_TEACHER;
+    if (f) atomicOr(err, f);
+    row_ok[r] = bad ? 0 : 1;
+  }
+  if (bad) return;
+
+  // Pass B: exponentials and their sum.
+  float sum = 0.f;
+  for (int k = tid; k < P2; k += kPrepThreads) {
+    const float e = (skey[k] != kNoIndex) ? ex2_approx(sval[k] - mx) : 0.f;
+    sval[k] = e;
+    sum += e;
+  }
+  sum = warp_sum(sum);
+  if (lane == 0) red_f[wid] = sum;
+  __syncthreads();
+  sum = 0.f;
+#pragma unroll
+  for (int w = 0; w < kPrepThreads / 32; ++w) sum += red_f[w];
+  __syncthreads();
+
+  // Pass C: probabilities, sum p ln p, sum p.
+  const float inv = 1.0f / sum;
+  const float lgsum = lg2_approx(sum);
+  float pl = 0.f, ps = 0.f;
+  for (int k = tid; k < P2; k += kPrepThreads) {
+    const float e = sval[k];
+    const float p = e * inv;
+    if (p > 0.f) {
+      // ln p = ln(e) - ln(sum) with ln(e) = log2(e) * ln 2
+      pl += p * (lg2_approx(e) - lgsum) * kLn2;
+    }
+    ps += p;
+    sval[k] = p;
+  }
+  pl = warp_sum(pl);
+  ps = warp_sum(ps);
+  if (lane == 0) {
+    red_f[wid] = pl;
+    red_i[wid] = __float_as_int(ps);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float a = 0.f, b = 0.f;
+#pragma unroll
+    for (int w = 0; w < kPrepThreads / 32; ++w) {
+      a += red_f[w];
+      b += __int_as_float(red_i[w]);
+    }
+    plogp[r] = a;
+    psum[r] = b;
+  }
+
+  // Bitonic sort of (key, p) by key over P2 (a power of two) slots.
+  for (int size = 2; size <= P2; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      __syncthreads();
+      for (int k = tid; k < P2; k += kPrepThreads) {
+        const int o = k ^ stride;
+        if (o > k) {
+          const bool up = (k & size) == 0;
+          const int a = skey[k], b = skey[o];
+          if ((a > b) == up) {
+            skey[k] = b;
+            skey[o] = a;
+            const float t = sval[k];
+            sval[k] = sval[o];
+            sval[o] = t;
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  for (int k = tid; k < K; k += kPrepThreads) {
+    idx_sorted[r * K + k] = skey[k];
+    p_sorted[r * K + k] = (skey[k] == kNoIndex) ? 0.f : sval[k];
+  }
+}
+
+// ------------------------------------------------------------- compaction
+// One block: rows[i] = the i-th row with row_ok != 0, n_valid = their count.
+constexpr int kScanThreads = 1024;
+
+__global__ void __launch_bounds__(kScanThreads) compact_kernel(const int32_t* __restrict__ row_ok,
+                                                              int64_t N,
+                                                              int32_t* __restrict__ rows,
+                                                              Ctrl* ctrl) {
+  __shared__ int warp_tot[kScanThreads / 32];
+  __shared__ int carry;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  if (tid == 0) carry = 0;
+  __syncthreads();
+  for (int64_t base = 0; base < N; base += kScanThreads) {
+    const int64_t r = base + tid;
+    const int f = (r < N && row_ok[r] != 0) ? 1 : 0;
+    const uint32_t bal = __ballot_sync(0xffffffffu, f);
+    const int before = __popc(bal & ((1u << lane) - 1u));
+    if (lane == 0) warp_tot[wid] = __popc(bal);
+    __syncthreads();
+    int off = 0, tot = 0;
+    for (int w = 0; w < kScanThreads / 32; ++w) {
+      const int c = warp_tot[w];
+      if (w < wid) off += c;
+      tot += c;
+    }
+    if (f) rows[carry + off + before] = static_cast<int32_t>(r);
+    __syncthreads();
+    if (tid == 0) carry += tot;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    ctrl->n_valid = carry;
+    ctrl->loss_sum = 0.0;
+  }
+}
+
+// ------------------------------------------------------------- per-chunk kernels
+
+// hc[i, :] = h[rows[row0 + i], :] for the chunk's valid rows; zero rows up to
+// the next multiple of 128 so the tensor-core tiles never read stale data.
+__global__ void gather_rows_kernel(const uint8_t* __restrict__ h, int64_t row_bytes,
+                                   ChunkArgs a, uint8_t* __restrict__ hc) {
+  const int i = blockIdx.x;
+  const int count = chunk_count(a.n_valid, a.row0, a.chunk);
+  if (i >= round_up(count, 128)) return;
+  uint4* dst = reinterpret_cast<uint4*>(hc + static_cast<int64_t>(i) * row_bytes);
+  const int64_t n16 = row_bytes / 16;
+  if (i < count) {
+    const int64_t r = a.rows[a.row0 + i];
+    const uint4* src = reinterpret_cast<const uint4*>(h + r * row_bytes);
+    for (int64_t j = threadIdx.x; j < n16; j += blockDim.x) dst[j] = src[j];
+  } else {
+    for (int64_t j = threadIdx.x; j < n16; j += blockDim.x) dst[j] = make_uint4(0, 0, 0, 0);
+  }
+}
+
+// boff[pb][i] = first position in row i's sorted list whose index is >= pb*128,
+// for pb = 0 .. n_pb (the last one is the number of kept entries).
+constexpr int kBoffRows = 64;
+constexpr int kBoffGroups = 4;
+constexpr int kBoffPerThread = 64;
+
+__global__ void __launch_bounds__(kBoffRows * kBoffGroups) bucket_offsets_kernel(ChunkArgs a) {
+  const int count = chunk_count(a.n_valid, a.row0, a.chunk);
+  const int i = blockIdx.x * kBoffRows + threadIdx.x;
+  if (i >= count) return;
+  const int pb0 = (blockIdx.y * kBoffGroups + threadIdx.y) * kBoffPerThread;
+  if (pb0 > a.n_pb) return;
+  const int pb1 = min(pb0 + kBoffPerThread, a.n_pb + 1);
+  const int32_t* lst = a.idx_sorted + static_cast<int64_t>(a.rows[a.row0 + i]) * a.K;
+  // lower bound of pb0 * 128
+  const int target0 = pb0 * kPB;
+  int lo = 0, hi = a.K;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(lst + mid) < target0) lo = mid + 1;
+    else hi = mid;
+  }
+  int off = lo;
+  for (int pb = pb0; pb < pb1; ++pb) {
+    const int target = pb * kPB;
+    while (off < a.K && __ldg(lst + off) < target) ++off;
+    a.boff[static_cast<int64_t>(pb) * a.cpad + i] = static_cast<uint16_t>(off);
+  }
+}
+
+// Combine the per-block statistics of each row of the chunk:
+//   lse2 = M + log2(sum_b l_b 2^(m_b - M)),  M = max_b m_b
+//   loss_i = plogp - ln2 * (sum_b ps_b - psum * lse2)
+// then overwrite part_m with alpha_b = 2^(m_b - lse2) / (T N_valid), the factor
+// that turns the stored exponentials of block b into softmax / (T N_valid).
+constexpr int kLseRows = 32;
+constexpr int kLseGroups = 16;
+
+__global__ void __launch_bounds__(kLseRows * kLseGroups) lse_kernel(
+    ChunkArgs a, const float* __restrict__ plogp, const float* __restrict__ psum, float T,
+    float* __restrict__ lse_out, float* __restrict__ loss_rows) {
+  __shared__ float sM[kLseGroups][kLseRows];
+  __shared__ float sL[kLseGroups][kLseRows];
+  __shared__ float sP[kLseGroups][kLseRows];
+  __shared__ float sLse[kLseRows];
+  const int count = chunk_count(a.n_valid, a.row0, a.chunk);
+  const int i0 = blockIdx.x * kLseRows;
+  if (i0 >= count) return;
+  const int x = threadIdx.x, y = threadIdx.y;
+  const int i = i0 + x;
+  const bool live = i < count;
+  float M = -INFINITY, L = 0.f, PS = 0.f;
+  if (live) {
+    for (int pb = y; pb < a.n_pb; pb += kLseGroups) {
+      const int64_t o = static_cast<int64_t>(pb) * a.cpad + i;
+      const float m = a.part_m[o], l = a.part_l[o];
+      PS += a.part_ps[o];
+      if (m > M) {
+        L = L * ex2_approx(M - m) + l;
+        M = m;
+      } else {
+        L += l * ex2_approx(m - M);
+      }
+    }
+  }
+  sM[y][x] = M;
+  sL[y][x] = L;
+  sP[y][x] = PS;
+  __syncthreads();
+  if (y == 0 && live) {
+    float MM = -INFINITY;
+    for (int g = 0; g < kLseGroups; ++g) MM = fmaxf(MM, sM[g][x]);
+    float LL = 0.f, PP = 0.f;
+    for (int g = 0; g < kLseGroups; ++g) {
+      LL += sL[g][x] * ex2_approx(sM[g][x] - MM);
+      PP += sP[g][x];
+    }
+    const float lse2 = MM + lg2_approx(LL);
+    const int64_t r = a.rows[a.row0 + i];
+    const float loss = plogp[r] - kLn2 * (PP - psum[r] * lse2);
+    lse_out[a.row0 + i] = lse2 * kLn2;
+    loss_rows[a.row0 + i] = loss;
+    sLse[x] = lse2;
+  }
+  __syncthreads();
+  if (!live) return;
+  const float lse2 = sLse[x];
+  const float scale = 1.0f / (T * static_cast<float>(*a.n_valid));
+  for (int pb = y; pb < a.n_pb; pb += kLseGroups) {
+    const int64_t o = static_cast<int64_t>(pb) * a.cpad + i;
+    a.part_m[o] = ex2_approx(a.part_m[o] - lse2) * scale;
+  }
+}
+
+// G[i, v] = u[i, v] * alpha_{block(v)} - (sum of p over teacher entries at v) / (T N_valid),
+// written in place over u.  Rows count .. round_up(count, 64) are zeroed (the
+// grad_W reduction reads whole 64-row blocks); columns >= V are zeroed.
+template <typename E>
+struct GVec;
+template <>
+struct GVec<uint16_t> {
+  static constexpr int kW = 8;
+  __device__ static void load(const uint16_t* p, float (&f)[8]) {
+    const uint4 v = *reinterpret_cast<const uint4*>(p);
+    f[0] = bf16lo_to_f32(v.x);
+    f[1] = bf16hi_to_f32(v.x);
+    f[2] = bf16lo_to_f32(v.y);
+    f[3] = bf16hi_to_f32(v.y);
+    f[4] = bf16lo_to_f32(v.z);
+    f[5] = bf16hi_to_f32(v.z);
+    f[6] = bf16lo_to_f32(v.w);
+    f[7] = bf16hi_to_f32(v.w);
+  }
+  __device__ static void store(uint16_t* p, const float (&f)[8]) {
+    *reinterpret_cast<uint4*>(p) = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                                              pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+  }
+};
+template <>
+struct GVec<float> {
+  static constexpr int kW = 4;
+  __device__ static void load(const float* p, float (&f)[4]) {
+    const float4 v = *reinterpret_cast<const float4*>(p);
+    f[0] = v.x;
+    f[1] = v.y;
+    f[2] = v.z;
+    f[3] = v.w;
+  }
+  __device__ static void store(float* p, const float (&f)[4]) {
+    *reinterpret_cast<float4*>(p) = make_float4(f[0], f[1], f[2], f[3]);
+  }
+};
+
+constexpr int kGThreads = 256;
+
+template <typename E>
+__global__ void __launch_bounds__(kGThreads) grad_tile_kernel(ChunkArgs a, E* __restrict__ g,
+                                                              float T) {
+  constexpr int W = GVec<E>::kW;
+  extern __shared__ uint8_t sm[];
+  float* salpha = reinterpret_cast<float*>(sm);
+  uint16_t* sboff = reinterpret_cast<uint16_t*>(salpha + a.n_pb);
+  const int count = chunk_count(a.n_valid, a.row0, a.chunk);
+  const int i = blockIdx.x;
+  if (i >= round_up(count, 64)) return;
+  E* row = g + static_cast<int64_t>(i) * a.ldg;
+  if (i >= count) {
+    float z[W];
+#pragma unroll
+    for (int j = 0; j < W; ++j) z[j] = 0.f;
+    for (int64_t v0 = static_cast<int64_t>(threadIdx.x) * W; v0 < a.ldg; v0 += kGThreads * W)
+      GVec<E>::store(row + v0, z);
+    return;
+  }
+  for (int pb = threadIdx.x; pb < a.n_pb; pb += kGThreads) {
+    salpha[pb] = a.part_m[static_cast<int64_t>(pb) * a.cpad + i];
+    sboff[pb] = a.boff[static_cast<int64_t>(pb) * a.cpad + i];
+  }
+  if (threadIdx.x == 0) sboff[a.n_pb] = a.boff[static_cast<int64_t>(a.n_pb) * a.cpad + i];
+  __syncthreads();
+  const int64_t r = a.rows[a.row0 + i];
+  const int32_t* lidx = a.idx_sorted + r * a.K;
+  const float* lp = a.p_sorted + r * a.K;
+  const float scale = 1.0f / (T * static_cast<float>(*a.n_valid));
+  for (int64_t v0 = static_cast<int64_t>(threadIdx.x) * W; v0 < a.ldg; v0 += kGThreads * W) {
+    float f[W];
+    if (v0 >= a.V) {
+#pragma unroll
+      for (int j = 0; j < W; ++j) f[j] = 0.f;
+    } else {
+      const int pb = static_cast<int>(v0 / kPB);
+      const float al = salpha[pb];
+      GVec<E>::load(row + v0, f);
+#pragma unroll
+      for (int j = 0; j < W; ++j) f[j] = (v0 + j < a.V) ? f[j] * al : 0.f;
+      const int e1 = sboff[pb + 1];
+      for (int e = sboff[pb]; e < e1; ++e) {
+        const int64_t c = static_cast<int64_t>(__ldg(lidx + e)) - v0;
+        if (c >= 0 && c < W) {
+          const float sub = __ldg(lp + e) * scale;
+#pragma unroll
+          for (int j = 0; j < W; ++j)
+            if (j == c) f[j] -= sub;
+        }
+      }
+    }
+    GVec<E>::store(row + v0, f);
+  }
+}
+
+// loss = (sum of the per-row terms, in fixed order, in fp64) / N_valid.
+constexpr int kFinThreads = 1024;
+
+__global__ void __launch_bounds__(kFinThreads) finalize_kernel(const float* __restrict__ loss_rows,
+                                                              Ctrl* ctrl, float* loss) {
+  __shared__ double sd[kFinThreads];
+  const int nv = ctrl->n_valid;
+  double s = 0.0;
+  for (int i = threadIdx.x; i < nv; i += kFinThreads) s += static_cast<double>(loss_rows[i]);
+  sd[threadIdx.x] = s;
+  __syncthreads();
+  for (int w = kFinThreads / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) sd[threadIdx.x] += sd[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    ctrl->loss_sum = sd[0];
+    *loss = nv > 0 ? static_cast<float>(sd[0] / static_cast<double>(nv)) : 0.f;
+  }
+}
+
+__global__ void zero_invalid_rows_kernel(const int32_t* __restrict__ row_ok, int64_t d,
+                                         float* __restrict__ grad_h) {
+  const int64_t r = blockIdx.x;
+  if (row_ok[r] != 0) return;
+  float* p = grad_h + r * d;
+  for (int64_t j = threadIdx.x; j < d; j += blockDim.x) p[j] = 0.f;
+}
+
+// ------------------------------------------------------------- fp32 CUDA-core path
+
+// Pass 1 on CUDA cores: a 32-row x 128-column tile of z = h_c W^T in fp32 FMA,
+// then the same per-block statistics and stored exponentials as the tensor
+// path (fp32 storage).
+constexpr int kSimtRows = 32;
+constexpr int kSimtKc = 32;
+
+__global__ void __launch_bounds__(256) simt_pass1_kernel(const float* __restrict__ hc,
+                                                        const float* __restrict__ W, int64_t d,
+                                                        ChunkArgs a, float k2,
+                                                        float* __restrict__ u) {
+  __shared__ float sA[kSimtRows][kSimtKc + 1];
+  __shared__ float sB[kPB][kSimtKc + 1];
+  __shared__ float sZ[kSimtRows][kPB + 1];
+  const int count = chunk_count(a.n_valid, a.row0, a.chunk);
+  const int i0 = blockIdx.y * kSimtRows;
+  if (i0 >= count) return;
+  const int pb = blockIdx.x;
+  const int col0 = pb * kPB;
+  const int tid = threadIdx.x, tx = tid & 31, ty = tid >> 5;
+  float acc[4][4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
+  for (int64_t k0 = 0; k0 < d; k0 += kSimtKc) {
+    for (int e = tid; e < kSimtRows * kSimtKc; e += 256) {
+      const int rr = e / kSimtKc, kk = e % kSimtKc;
+      const int64_t gi = i0 + rr, gk = k0 + kk;
+      sA[rr][kk] = (gi < count && gk < d) ? hc[gi * d + gk] : 0.f;
+    }
+    for (int e = tid; e < kPB * kSimtKc; e += 256) {
+      const int cc = e / kSimtKc, kk = e % kSimtKc;
+      const int64_t gv = col0 + cc, gk = k0 + kk;
+      sB[cc][kk] = (gv < a.V && gk < d) ? W[gv * d + gk] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int kk = 0; kk < kSimtKc; ++kk) {
+      float av[4], bv[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) av[r] = sA[ty * 4 + r][kk];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) bv[c] = sB[tx + 32 * c][kk];
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(av[r], bv[c], acc[r][c]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) sZ[ty * 4 + r][tx + 32 * c] = acc[r][c];
+  __syncthreads();
+  // warp ty handles rows ty*4 .. ty*4+3; lane tx covers columns tx + 32c
+  const int nv = min(kPB, a.V - col0);
+  for (int r = 0; r < 4; ++r) {
+    const int li = ty * 4 + r;
+    const int i = i0 + li;
+    if (i >= count) break;
+    float mx = -INFINITY;
+    for (int c = tx; c < nv; c += 32) mx = fmaxf(mx, sZ[li][c]);
+    mx = warp_max(mx);
+    const float m2 = mx * k2;
+    float l = 0.f;
+    float* urow = u + static_cast<int64_t>(i) * a.ldg + col0;
+    for (int c = tx; c < kPB; c += 32) {
+      const float e = (c < nv) ? ex2_approx(fmaf(sZ[li][c], k2, -m2)) : 0.f;
+      l += e;
+      urow[c] = e;
+    }
+    l = warp_sum(l);
+    float ps = 0.f;
+    const int64_t orow = a.rows[a.row0 + i];
+    const int lo = a.boff[static_cast<int64_t>(pb) * a.cpad + i];
+    const int hi = a.boff[static_cast<int64_t>(pb + 1) * a.cpad + i];
+    for (int e = lo + tx; e < hi; e += 32) {
+      const int c = (a.idx_sorted[orow * a.K + e] - col0) & (kPB - 1);
+      ps += a.p_sorted[orow * a.K + e] * sZ[li][c];
+    }
+    ps = warp_sum(ps);
+    if (tx == 0) {
+      const int64_t o = static_cast<int64_t>(pb) * a.cpad + i;
+      a.part_m[o] = m2;
+      a.part_l[o] = l;
+      a.part_ps[o] = ps * k2;
+    }
+  }
+}
+
+// Generic fp32 GEMM on CUDA cores (64 x 64 tiles, 4 x 4 outputs per thread).
+constexpr int kGT = 64;
+constexpr int kGK = 16;
+
+__global__ void __launch_bounds__(256) simt_gemm_kernel(SimtGemm g) {
+  __shared__ float sA[kGK][kGT + 1];
+  __shared__ float sB[kGK][kGT + 1];
+  int64_t M = g.M_cap, K = g.Kfix;
+  if (g.n_valid != nullptr) {
+    long long c = static_cast<long long>(*g.n_valid) - g.row0;
+    if (c < 0) c = 0;
+    if (g.m_from_count) M = c < M ? c : M;
+    if (g.k_from_count) K = c < K ? c : K;
+  }
+  if (K == 0 && g.accumulate) return;
+  const int64_t m0 = static_cast<int64_t>(blockIdx.y) * kGT;
+  const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kGT;
+  if (m0 >= M) return;
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  float acc[4][4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
+  for (int64_t k0 = 0; k0 < K; k0 += kGK) {
+    for (int e = tid; e < kGT * kGK; e += 256) {
+      const int kk = e % kGK, mm = e / kGK;
+      const int64_t gm = m0 + mm, gk = k0 + kk;
+      sA[kk][mm] = (gm < M && gk < K) ? g.A[gm * g.sam + gk * g.sak] : 0.f;
+    }
+    for (int e = tid; e < kGT * kGK; e += 256) {
+      const int nn = e % kGT, kk = e / kGT;
+      const int64_t gn = n0 + nn, gk = k0 + kk;
+      sB[kk][nn] = (gn < g.N && gk < K) ? g.B[gk * g.sbk + gn * g.sbn] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < kGK; ++kk) {
+      float av[4], bv[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) av[r] = sA[kk][ty * 4 + r];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) bv[c] = sB[kk][tx + 16 * c];
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(av[r], bv[c], acc[r][c]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int64_t gm = m0 + ty * 4 + r;
+    if (gm >= M) continue;
+    const int64_t orow = g.row_map != nullptr ? g.row_map[g.row_map_off + gm] : gm;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int64_t gn = n0 + tx + 16 * c;
+      if (gn >= g.N) continue;
+      float* p = g.C + orow * g.ldc + gn;
+      *p = g.accumulate ? *p + acc[r][c] : acc[r][c];
+    }
+  }
+}
+
+int next_pow2(int x) {
+  int p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ launchers
+
+cudaError_t launch_teacher_prep(const int32_t* idx, const float* logit, const uint8_t* mask,
+                                int64_t N, int K, int64_t V, float T, int32_t* row_ok,
+                                int32_t* idx_sorted, float* p_sorted, float* plogp, float* psum,
+                                uint32_t* err, cudaStream_t s) {
+  if (N == 0) return cudaSuccess;
+  const int P2 = next_pow2(K < 2 ? 2 : K);
+  const size_t smem = static_cast<size_t>(P2) * 8;
+  cudaError_t e = cudaFuncSetAttribute(teacher_prep_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem < 48 * 1024 ? 48 * 1024 : smem));
+  if (e != cudaSuccess) return e;
+  teacher_prep_kernel<<<static_cast<unsigned>(N), kPrepThreads, smem, s>>>(
+      idx, logit, mask, K, V, kLog2e / T, P2, row_ok, idx_sorted, p_sorted, plogp, psum, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_compact(const int32_t* row_ok, int64_t N, int32_t* rows, Ctrl* ctrl,
+                           cudaStream_t s) {
+  compact_kernel<<<1, kScanThreads, 0, s>>>(row_ok, N, rows, ctrl);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const void* h, size_t elem, int64_t d, const ChunkArgs& a,
+                               void* hc, cudaStream_t s) {
+  gather_rows_kernel<<<static_cast<unsigned>(round_up(a.chunk, 128)), 128, 0, s>>>(
+      static_cast<const uint8_t*>(h), d * static_cast<int64_t>(elem), a,
+      static_cast<uint8_t*>(hc));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bucket_offsets(const ChunkArgs& a, cudaStream_t s) {
+  const dim3 block(kBoffRows, kBoffGroups);
+  const dim3 grid(static_cast<unsigned>(ceil_div(a.chunk, kBoffRows)),
+                  static_cast<unsigned>(ceil_div(a.n_pb + 1, kBoffGroups * kBoffPerThread)));
+  bucket_offsets_kernel<<<grid, block, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lse(const ChunkArgs& a, const float* plogp, const float* psum, float T,
+                       float* lse, float* loss_rows, cudaStream_t s) {
+  const dim3 block(kLseRows, kLseGroups);
+  lse_kernel<<<static_cast<unsigned>(ceil_div(a.chunk, kLseRows)), block, 0, s>>>(
+      a, plogp, psum, T, lse, loss_rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_grad_tile(const ChunkArgs& a, void* g, size_t elem, float T, cudaStream_t s) {
+  const size_t smem = static_cast<size_t>(a.n_pb) * 4 + static_cast<size_t>(a.n_pb + 1) * 2 + 16;
+  const unsigned grid = static_cast<unsigned>(round_up(a.chunk, 64));
+  cudaError_t e;
+  if (elem == 2) {
+    e = cudaFuncSetAttribute(grad_tile_kernel<uint16_t>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem < 48 * 1024 ? 48 * 1024 : smem));
+    if (e != cudaSuccess) return e;
+    grad_tile_kernel<uint16_t><<<grid, kGThreads, smem, s>>>(a, static_cast<uint16_t*>(g), T);
+  } else {
+    e = cudaFuncSetAttribute(grad_tile_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem < 48 * 1024 ? 48 * 1024 : smem));
+    if (e != cudaSuccess) return e;
+    grad_tile_kernel<float><<<grid, kGThreads, smem, s>>>(a, static_cast<float*>(g), T);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(const float* loss_rows, Ctrl* ctrl, float* loss, cudaStream_t s) {
+  finalize_kernel<<<1, kFinThreads, 0, s>>>(loss_rows, ctrl, loss);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_zero_invalid_rows(const int32_t* row_ok, int64_t N, int64_t d, float* grad_h,
+                                     cudaStream_t s) {
+  if (N == 0) return cudaSuccess;
+  zero_invalid_rows_kernel<<<static_cast<unsigned>(N), 128, 0, s>>>(row_ok, d, grad_h);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_simt_pass1(const float* hc, const float* W, int64_t d, const ChunkArgs& a,
+                              float k2, float* u, cudaStream_t s) {
+  const dim3 grid(static_cast<unsigned>(a.n_pb), static_cast<unsigned>(ceil_div(a.chunk, kSimtRows)));
+  simt_pass1_kernel<<<grid, 256, 0, s>>>(hc, W, d, a, k2, u);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_simt_gemm(const SimtGemm& g, cudaStream_t s) {
+  const dim3 grid(static_cast<unsigned>(ceil_div(g.N, kGT)),
+                  static_cast<unsigned>(ceil_div(g.M_cap, kGT)));
+  if (grid.x == 0 || grid.y == 0) return cudaSuccess;
+  simt_gemm_kernel<<<grid, 256, 0, s>>>(g);
+  return cudaGetLastError();
+}
+
+}  // namespace kd

@@ -1,0 +1,684 @@
+// kd_tc_gemm.cu -- the tensor-core kernels of the fused top-K KL loss.
+//
+// One persistent, warp-specialised kernel template runs every contraction of
+// the loss on the tcgen05 tensor cores ("Efficient Knowledge Distillation for
+// LLMs: Offline Top-K Logits and a Fused Chunked KL Loss", ai2day.live story,
+// "What did the researchers change?": the student logits are produced and
+// consumed one chunk of the sequence at a time, never as the full grid):
+//
+//   pass 1   z = h_c W^T for one token chunk (M = chunk rows, N = V, K = d),
+//            with an epilogue that turns each 128 x 128 quarter of the fp32
+//            accumulator into logsumexp statistics (block max, sum of
+//            exponentials, teacher-weighted logit sum) and stores the
+//            normalised exponentials u = 2^(s2 - m2) as bf16;
+//   backward grad_h rows of the chunk = G_c W   (M = chunk, N = d, K = V) and
+//            grad_W (+)= G_c^T h_c              (M = V, N = d, K = chunk),
+//            both in the same launch, fp32 results stored or accumulated.
+//
+// CTA layout (320 threads, one CTA per SM):
+//   warp 0      TMA producer: takes tile numbers from a global counter, hands
+//               them to the other roles through a shared-memory ring, and
+//               streams 64-deep K blocks of A and B into a 4-stage ring;
+//   warp 1      allocates TMEM (two 128 x 256 fp32 accumulators) and issues
+//               tcgen05.mma (128 x 256 x 16, bf16 in, fp32 out) from one lane;
+//   warps 2-9   epilogue: each warp reads 32 TMEM lanes (rows) x 128 columns.
+// Operands are staged in the 128-byte swizzle layout; a K-major operand tile
+// is one TMA box of 64 x rows, an MN-major tile is made of 64 x 64 boxes.
+// Every wait is time-bounded (kd_ptx.cuh): on a timeout the CTA records
+// KD_FLAG_TIMEOUT, drains its in-flight copies and MMAs, frees TMEM and exits.
+#include <math.h>
+#include <string.h>
+
+#include "kd_internal.h"
+#include "kd_ptx.cuh"
+
+namespace kd {
+namespace {
+
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = (2 + kEpiWarps) * 32;
+constexpr int kSched = 4;
+constexpr uint32_t kTmemCols = 2 * kBN;
+constexpr int kABytes = kBM * kBK * 2;
+constexpr int kBBytes = kBN * kBK * 2;
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kAtomBytes = 64 * kBK * 2;  // one 64 (MN) x 64 (K) box of an MN-major tile
+
+struct Ctl {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t sfull[kSched];
+  uint64_t sempty[kSched];
+  uint64_t drain;
+  int sched_tile[kSched];
+  uint32_t tmem_base;
+  int abort;
+};
+
+constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStages) * kStageBytes + sizeof(Ctl);
+
+enum : int { kModePass1 = 0, kModeStore = 1 };
+
+struct KParams {
+  CUtensorMap tmA[2];
+  CUtensorMap tmB[2];
+  int a_mn[2], b_mn[2];
+  int M[2], N[2], K[2];
+  float* out[2];
+  int64_t ldo[2];
+  int vec_ok[2];
+  const int32_t* row_map[2];
+  int64_t row_map_off[2];
+  int accumulate[2];
+  int count_mode[2];
+  int nprob;
+  const int32_t* n_valid;
+  int64_t row0;
+  int chunk;
+  uint32_t* counter;
+  uint32_t* err;
+  // pass-1 epilogue
+  float k2;
+  int V;
+  int64_t cpad;
+  int n_pb;
+  int K_top;
+  const int32_t* rows;
+  const int32_t* idx_sorted;
+  const float* p_sorted;
+  const uint16_t* boff;
+  float* part_m;
+  float* part_l;
+  float* part_ps;
+  uint16_t* u;
+  int64_t ldg;
+};
+
+struct Sizes {
+  int M[2], N[2], nkb[2], mt[2], nt[2], tiles[2];
+  int total;
+  int count;
+};
+
+__device__ __forceinline__ Sizes get_sizes(const KParams& P) {
+  Sizes s;
+  int count = P.chunk;
+  if (P.n_valid != nullptr) {
+    const long long c = static_cast<long long>(*P.n_valid) - P.row0;
+    count = c < 0 ? 0 : (c > P.chunk ? P.chunk : static_cast<int>(c));
+  }
+  s.count = count;
+  s.total = 0;
+#pragma unroll
+  for (int pi = 0; pi < 2; ++pi) {
+    int M = P.M[pi], N = P.N[pi], K = P.K[pi];
+    if (P.count_mode[pi] == 1) M = min(M, count);
+    if (P.count_mode[pi] == 2) K = min(K, count);
+    s.M[pi] = M;
+    s.N[pi] = N;
+    s.nkb[pi] = (K + kBK - 1) / kBK;
+    s.mt[pi] = (M + kBM - 1) / kBM;
+    s.nt[pi] = (N + kBN - 1) / kBN;
+    int tiles = s.mt[pi] * s.nt[pi];
+    if (pi >= P.nprob) tiles = 0;
+    // Nothing to add: an accumulating problem with an empty reduction.
+    if (s.nkb[pi] == 0 && P.accumulate[pi]) tiles = 0;
+    s.tiles[pi] = tiles;
+    s.total += tiles;
+  }
+  return s;
+}
+
+struct Tile {
+  int prob, m, n, nkb;
+};
+
+// Pass 1 walks the vocabulary slowly (m fastest) so that the CTAs running at
+// the same time share one W tile; the backward walks the output columns
+// fastest so that the CTAs running together share one A (G) slab.
+template <int MODE>
+__device__ __forceinline__ Tile decode_tile(const Sizes& S, int t) {
+  Tile tl;
+  tl.prob = 0;
+  if (t >= S.tiles[0]) {
+    tl.prob = 1;
+    t -= S.tiles[0];
+  }
+  const int pi = tl.prob;
+  if (MODE == kModePass1) {
+    tl.m = t % S.mt[pi];
+    tl.n = t / S.mt[pi];
+  } else {
+    tl.n = t % S.nt[pi];
+    tl.m = t / S.nt[pi];
+  }
+  tl.nkb = S.nkb[pi];
+  return tl;
+}
+
+__device__ __forceinline__ uint8_t* align_smem(uint8_t* raw) {
+  const uint32_t a = smem_u32(raw);
+  return raw + (((a + 1023u) & ~1023u) - a);
+}
+
+// Takes the next tile number from the shared ring (all lanes of the calling
+// warp, or a single thread).  Returns false when the CTA has to stop.
+__device__ __forceinline__ bool sched_pop(Ctl* ctl, int& slot, uint32_t& sphase, int& t,
+                                          const WaitCtx& wc) {
+  if (!mbar_wait(&ctl->sfull[slot], sphase, wc)) return false;
+  t = *reinterpret_cast<volatile int*>(&ctl->sched_tile[slot]);
+  return true;
+}
+
+template <int MODE>
+__device__ void producer_loop(const KParams& P, const Sizes& S, uint8_t* smem, Ctl* ctl,
+                              const WaitCtx& wc) {
+  int stage = 0;
+  uint32_t phase = 0;
+  int slot = 0;
+  uint32_t sphase = 0;
+  uint32_t issued[kStages];
+#pragma unroll
+  for (int s = 0; s < kStages; ++s) issued[s] = 0;
+  bool aborted = false;
+  while (true) {
+    if (!mbar_wait(&ctl->sempty[slot], sphase ^ 1u, wc)) {
+      aborted = true;
+      break;
+    }
+    int t = static_cast<int>(atomicAdd(P.counter, 1u));
+    if (t >= S.total) t = -1;
+    *reinterpret_cast<volatile int*>(&ctl->sched_tile[slot]) = t;
+    mbar_arrive(&ctl->sfull[slot]);
+    if (++slot == kSched) {
+      slot = 0;
+      sphase ^= 1u;
+    }
+    if (t < 0) break;
+    const Tile tl = decode_tile<MODE>(S, t);
+    const int pi = tl.prob;
+    const CUtensorMap* ma = &P.tmA[pi];
+    const CUtensorMap* mb = &P.tmB[pi];
+    for (int kb = 0; kb < tl.nkb; ++kb) {
+      if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, wc)) {
+        aborted = true;
+        break;
+      }
+      uint8_t* sa = smem + stage * kStageBytes;
+      uint8_t* sb = sa + kABytes;
+      uint64_t* fb = &ctl->full[stage];
+      mbar_arrive_expect_tx(fb, kStageBytes);
+      const int k0 = kb * kBK;
+      if (P.a_mn[pi]) {
+#pragma unroll
+        for (int a = 0; a < kBM / 64; ++a) tma_load_2d(sa + a * kAtomBytes, ma, fb, tl.m * kBM + a * 64, k0);
+      } else {
+        tma_load_2d(sa, ma, fb, k0, tl.m * kBM);
+      }
+      if (P.b_mn[pi]) {
+#pragma unroll
+        for (int a = 0; a < kBN / 64; ++a) tma_load_2d(sb + a * kAtomBytes, mb, fb, tl.n * kBN + a * 64, k0);
+      } else {
+        tma_load_2d(sb, mb, fb, k0, tl.n * kBN);
+      }
+      issued[stage] += 1;
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    if (aborted) break;
+  }
+  if (aborted) {
+    // Let the copies already issued land before the CTA's shared memory goes away.
+#pragma unroll
+    for (int s = 0; s < kStages; ++s)
+      if (issued[s] != 0) mbar_wait_drain(&ctl->full[s], (issued[s] - 1u) & 1u, P.err);
+  }
+}
+
+template <int MODE>
+__device__ void mma_loop(const KParams& P, const Sizes& S, uint8_t* smem, Ctl* ctl, uint32_t tmem,
+                         const WaitCtx& wc) {
+  int stage = 0;
+  uint32_t phase = 0;
+  int slot = 0;
+  uint32_t sphase = 0;
+  int it = 0;
+  while (true) {
+    int t;
+    if (!sched_pop(ctl, slot, sphase, t, wc)) break;
+    mbar_arrive(&ctl->sempty[slot]);
+    if (++slot == kSched) {
+      slot = 0;
+      sphase ^= 1u;
+    }
+    if (t < 0) break;
+    const Tile tl = decode_tile<MODE>(S, t);
+    const int b = it & 1;
+    const uint32_t tp = (static_cast<uint32_t>(it) >> 1) & 1u;
+    ++it;
+    if (!mbar_wait(&ctl->tempty[b], tp ^ 1u, wc)) break;
+    tc_fence_after();
+    const uint32_t d_tmem = tmem + static_cast<uint32_t>(b * kBN);
+    const int pi = tl.prob;
+    const int a_mn = P.a_mn[pi], b_mn = P.b_mn[pi];
+    const uint32_t idesc = idesc_bf16_f32(kBM, kBN, a_mn, b_mn);
+    bool ok = true;
+    for (int kb = 0; kb < tl.nkb; ++kb) {
+      if (!mbar_wait(&ctl->full[stage], phase, wc)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t sa = smem_u32(smem + stage * kStageBytes);
+      const uint32_t sb = sa + kABytes;
+#pragma unroll
+      for (int kk = 0; kk < kBK / 16; ++kk) {
+        // K-major: the next 16 K elements are 32 bytes further along each
+        // 128-byte row.  MN-major: they are the next 16 rows of 128 bytes.
+        const uint64_t ad = a_mn ? sdesc_sw128(sa + kk * 2048, kAtomBytes, 1024)
+                                 : sdesc_sw128(sa + kk * 32, 16, 1024);
+        const uint64_t bd = b_mn ? sdesc_sw128(sb + kk * 2048, kAtomBytes, 1024)
+                                 : sdesc_sw128(sb + kk * 32, 16, 1024);
+        umma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+      }
+      umma_commit(&ctl->empty[stage]);
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    if (!ok) break;
+    umma_commit(&ctl->tfull[b]);
+  }
+  // Every MMA this thread issued must finish before TMEM is freed.
+  umma_commit(&ctl->drain);
+  mbar_wait_drain(&ctl->drain, 0, P.err);
+}
+
+// ------------------------------------------------------------------ epilogues
+
+__device__ __forceinline__ void load_acc128(uint32_t ta, float (&v0)[32], float (&v1)[32],
+                                            float (&v2)[32], float (&v3)[32]) {
+  tmem_ld_x32(ta, v0);
+  tmem_ld_x32(ta + 32, v1);
+  tmem_ld_x32(ta + 64, v2);
+  tmem_ld_x32(ta + 96, v3);
+  tmem_ld_wait();
+  reg_fence(v0);
+  reg_fence(v1);
+  reg_fence(v2);
+  reg_fence(v3);
+}
+
+__device__ __forceinline__ void store_chunk32(float* dst, const float (&v)[32], int nc, bool vec,
+                                              bool acc) {
+  if (vec && nc >= 32) {
+    float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float4 x = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      if (acc) {
+        const float4 o = d4[j];
+        x.x += o.x;
+        x.y += o.y;
+        x.z += o.z;
+        x.w += o.w;
+      }
+      d4[j] = x;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (j < nc) dst[j] = acc ? dst[j] + v[j] : v[j];
+    }
+  }
+}
+
+__device__ void epilogue_store(const KParams& P, const Sizes& S, Ctl* ctl, uint32_t tmem,
+                               const WaitCtx& wc, int warp, int lane) {
+  const int q = warp & 3;           // TMEM lane quarter this warp may read
+  const int half = (warp - 2) >> 2; // which 128 columns of the 256
+  int slot = 0;
+  uint32_t sphase = 0;
+  int it = 0;
+  while (true) {
+    int t = -1;
+    bool ok = sched_pop(ctl, slot, sphase, t, wc);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) break;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl->sempty[slot]);
+    if (++slot == kSched) {
+      slot = 0;
+      sphase ^= 1u;
+    }
+    if (t < 0) break;
+    const Tile tl = decode_tile<kModeStore>(S, t);
+    const int b = it & 1;
+    const uint32_t tp = (static_cast<uint32_t>(it) >> 1) & 1u;
+    ++it;
+    ok = mbar_wait(&ctl->tfull[b], tp, wc);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) break;
+    tc_fence_after();
+    const int pi = tl.prob;
+    float v0[32], v1[32], v2[32], v3[32];
+    if (tl.nkb > 0) {
+      const uint32_t ta = tmem + (static_cast<uint32_t>(q * 32) << 16) +
+                          static_cast<uint32_t>(b * kBN + half * 128);
+      load_acc128(ta, v0, v1, v2, v3);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v0[j] = v1[j] = v2[j] = v3[j] = 0.f;
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl->tempty[b]);
+
+    const int i = tl.m * kBM + q * 32 + lane;
+    const int col0 = tl.n * kBN + half * 128;
+    if (i < S.M[pi] && col0 < S.N[pi]) {
+      const int64_t orow =
+          P.row_map[pi] != nullptr ? P.row_map[pi][P.row_map_off[pi] + i] : static_cast<int64_t>(i);
+      float* dst = P.out[pi] + orow * P.ldo[pi] + col0;
+      const int nc = min(128, S.N[pi] - col0);
+      const bool vec = P.vec_ok[pi] != 0;
+      const bool acc = P.accumulate[pi] != 0;
+      store_chunk32(dst, v0, nc, vec, acc);
+      if (nc > 32) store_chunk32(dst + 32, v1, nc - 32, vec, acc);
+      if (nc > 64) store_chunk32(dst + 64, v2, nc - 64, vec, acc);
+      if (nc > 96) store_chunk32(dst + 96, v3, nc - 96, vec, acc);
+    }
+  }
+}
+
+// Logsumexp statistics of 32 consecutive logits of one row, in base-2 units
+// s2 = z * k2 relative to the block max m2; exponentials stored as bf16.
+template <bool kMasked>
+__device__ __forceinline__ void lse_chunk32(const float (&v)[32], int nvalid, float k2, float m2,
+                                            float& l, uint16_t* dst) {
+  uint32_t w[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    float e0 = ex2_approx(fmaf(v[2 * j], k2, -m2));
+    float e1 = ex2_approx(fmaf(v[2 * j + 1], k2, -m2));
+    if (kMasked) {
+      e0 = (2 * j < nvalid) ? e0 : 0.f;
+      e1 = (2 * j + 1 < nvalid) ? e1 : 0.f;
+    }
+    l += e0 + e1;
+    w[j] = pack_bf16x2(e0, e1);
+  }
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) d4[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+}
+
+__device__ __forceinline__ float max32(const float (&v)[32], int nvalid, bool masked) {
+  float m = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    if (!masked || j < nvalid) m = fmaxf(m, v[j]);
+  }
+  return m;
+}
+
+__device__ void epilogue_pass1(const KParams& P, const Sizes& S, Ctl* ctl, uint32_t tmem,
+                               const WaitCtx& wc, int warp, int lane) {
+  const int q = warp & 3;
+  const int half = (warp - 2) >> 2;
+  int slot = 0;
+  uint32_t sphase = 0;
+  int it = 0;
+  const float k2 = P.k2;
+  while (true) {
+    int t = -1;
+    bool ok = sched_pop(ctl, slot, sphase, t, wc);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) break;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl->sempty[slot]);
+    if (++slot == kSched) {
+      slot = 0;
+      sphase ^= 1u;
+    }
+    if (t < 0) break;
+    const Tile tl = decode_tile<kModePass1>(S, t);
+    const int b = it & 1;
+    const uint32_t tp = (static_cast<uint32_t>(it) >> 1) & 1u;
+    ++it;
+
+    const int i = tl.m * kBM + q * 32 + lane;  // row within the chunk
+    const int col0 = tl.n * kBN + half * 128;  // first vocabulary column of this block
+    const int pb = tl.n * 2 + half;            // 128-column block index
+    const bool live = (i < S.count) && (pb < P.n_pb);
+    // Teacher entries of this row that fall in this column block.
+    int lo = 0, hi = 0;
+    const int32_t* lidx = nullptr;
+    const float* lp = nullptr;
+    if (live) {
+      lo = P.boff[static_cast<int64_t>(pb) * P.cpad + i];
+      hi = P.boff[static_cast<int64_t>(pb + 1) * P.cpad + i];
+      const int64_t r = P.rows[P.row0 + i];
+      lidx = P.idx_sorted + r * P.K_top;
+      lp = P.p_sorted + r * P.K_top;
+    }
+
+    ok = mbar_wait(&ctl->tfull[b], tp, wc);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) break;
+    tc_fence_after();
+    const uint32_t ta = tmem + (static_cast<uint32_t>(q * 32) << 16) +
+                        static_cast<uint32_t>(b * kBN + half * 128);
+    float v0[32], v1[32], v2[32], v3[32];
+    load_acc128(ta, v0, v1, v2, v3);
+
+    // Logits at the teacher's indices: the warp walks its lanes' pending
+    // entries one at a time, each a single-column TMEM load.
+    float ps = 0.f;
+    uint32_t pend = __ballot_sync(0xffffffffu, lo < hi);
+    while (pend != 0u) {
+      const int src = __ffs(pend) - 1;
+      int jj = 0;
+      if (lo < hi) jj = lidx[lo] - col0;
+      const int j = __shfl_sync(0xffffffffu, jj, src) & 127;
+      float z = tmem_ld_x1(ta + static_cast<uint32_t>(j));
+      tmem_ld_wait();
+      reg_fence1(z);
+      if (lane == src) {
+        ps = fmaf(lp[lo], z, ps);
+        ++lo;
+      }
+      pend = __ballot_sync(0xffffffffu, lo < hi);
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl->tempty[b]);
+
+    if (live) {
+      const int nv = min(128, P.V - col0);
+      uint16_t* dst = P.u + static_cast<int64_t>(i) * P.ldg + col0;
+      float l = 0.f;
+      float m2;
+      if (nv == 128) {
+        const float mx = fmaxf(fmaxf(max32(v0, 32, false), max32(v1, 32, false)),
+                               fmaxf(max32(v2, 32, false), max32(v3, 32, false)));
+        m2 = mx * k2;
+        lse_chunk32<false>(v0, 32, k2, m2, l, dst);
+        lse_chunk32<false>(v1, 32, k2, m2, l, dst + 32);
+        lse_chunk32<false>(v2, 32, k2, m2, l, dst + 64);
+        lse_chunk32<false>(v3, 32, k2, m2, l, dst + 96);
+      } else {
+        const float mx = fmaxf(fmaxf(max32(v0, nv, true), max32(v1, nv - 32, true)),
+                               fmaxf(max32(v2, nv - 64, true), max32(v3, nv - 96, true)));
+        m2 = mx * k2;
+        lse_chunk32<true>(v0, nv, k2, m2, l, dst);
+        lse_chunk32<true>(v1, nv - 32, k2, m2, l, dst + 32);
+        lse_chunk32<true>(v2, nv - 64, k2, m2, l, dst + 64);
+        lse_chunk32<true>(v3, nv - 96, k2, m2, l, dst + 96);
+      }
+      const int64_t o = static_cast<int64_t>(pb) * P.cpad + i;
+      P.part_m[o] = m2;
+      P.part_l[o] = l;
+      P.part_ps[o] = ps * k2;
+    }
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ KParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align_smem(smem_raw);
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + kStages * kStageBytes);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const Sizes S = get_sizes(P);
+  if (S.total == 0) return;
+
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&ctl->full[s], 1);
+      mbar_init(&ctl->empty[s], 1);
+    }
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&ctl->tfull[b], 1);
+      mbar_init(&ctl->tempty[b], kEpiWarps);
+    }
+#pragma unroll
+    for (int s = 0; s < kSched; ++s) {
+      mbar_init(&ctl->sfull[s], 1);
+      mbar_init(&ctl->sempty[s], 1 + kEpiWarps);
+    }
+    mbar_init(&ctl->drain, 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&P.tmA[0]);
+    tma_prefetch_desc(&P.tmB[0]);
+    if (P.nprob > 1) {
+      tma_prefetch_desc(&P.tmA[1]);
+      tma_prefetch_desc(&P.tmB[1]);
+    }
+  }
+  if (warp == 1) tmem_alloc(&ctl->tmem_base, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  const WaitCtx wc{&ctl->abort, P.err};
+
+  if (warp == 0) {
+    if (lane == 0) producer_loop<MODE>(P, S, smem, ctl, wc);
+  } else if (warp == 1) {
+    if (lane == 0) mma_loop<MODE>(P, S, smem, ctl, tmem, wc);
+  } else {
+    if (MODE == kModePass1)
+      epilogue_pass1(P, S, ctl, tmem, wc, warp, lane);
+    else
+      epilogue_store(P, S, ctl, tmem, wc, warp, lane);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int MODE>
+cudaError_t launch_mode(const KParams& P, int grid, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<MODE>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return e;
+  tc_gemm_kernel<MODE><<<grid, kThreads, kSmemBytes, s>>>(P);
+  return cudaGetLastError();
+}
+
+bool encode_operand(CUtensorMap* m, const void* base, int mn, int64_t inner, int64_t outer,
+                    int64_t ld, int rows_per_tile) {
+  if (mn) return encode_tmap_bf16(m, base, inner, outer, ld, 64, kBK);
+  return encode_tmap_bf16(m, base, inner, outer, ld, kBK, rows_per_tile);
+}
+
+}  // namespace
+
+cudaError_t launch_tc_gemm(const TcGemmArgs& g, cudaStream_t s) {
+  KParams P;
+  memset(&P, 0, sizeof(P));
+  for (int pi = 0; pi < g.nprob; ++pi) {
+    const TcProblem& q = g.pr[pi];
+    if (!encode_operand(&P.tmA[pi], q.A, q.a_mn, q.a_inner, q.a_outer, q.lda, kBM) ||
+        !encode_operand(&P.tmB[pi], q.B, q.b_mn, q.b_inner, q.b_outer, q.ldb, kBN))
+      return cudaErrorInvalidValue;
+    P.a_mn[pi] = q.a_mn;
+    P.b_mn[pi] = q.b_mn;
+    P.M[pi] = static_cast<int>(q.M);
+    P.N[pi] = static_cast<int>(q.N);
+    P.K[pi] = static_cast<int>(q.K);
+    P.out[pi] = q.out;
+    P.ldo[pi] = q.ldo;
+    P.vec_ok[pi] = (q.ldo % 4 == 0) && (reinterpret_cast<uintptr_t>(q.out) % 16 == 0);
+    P.row_map[pi] = q.row_map;
+    P.row_map_off[pi] = q.row_map_off;
+    P.accumulate[pi] = q.accumulate;
+    P.count_mode[pi] = q.count_mode;
+  }
+  if (g.nprob == 1) P.tmA[1] = P.tmA[0], P.tmB[1] = P.tmB[0];
+  P.nprob = g.nprob;
+  P.n_valid = g.n_valid;
+  P.row0 = g.row0;
+  P.chunk = g.chunk;
+  P.counter = g.counter;
+  P.err = g.err;
+  cudaError_t e = cudaMemsetAsync(g.counter, 0, sizeof(uint32_t), s);
+  if (e != cudaSuccess) return e;
+  return launch_mode<kModeStore>(P, g.num_sms, s);
+}
+
+cudaError_t launch_tc_pass1(const Pass1Args& p, const ChunkArgs& a, cudaStream_t s) {
+  KParams P;
+  memset(&P, 0, sizeof(P));
+  if (!encode_operand(&P.tmA[0], p.hc, 0, p.d, a.cpad, p.d, kBM) ||
+      !encode_operand(&P.tmB[0], p.W, 0, p.d, a.V, p.d, kBN))
+    return cudaErrorInvalidValue;
+  P.tmA[1] = P.tmA[0];
+  P.tmB[1] = P.tmB[0];
+  P.M[0] = a.chunk;
+  P.N[0] = a.V;
+  P.K[0] = static_cast<int>(p.d);
+  P.count_mode[0] = 1;
+  P.nprob = 1;
+  P.n_valid = a.n_valid;
+  P.row0 = a.row0;
+  P.chunk = a.chunk;
+  P.counter = p.counter;
+  P.err = p.err;
+  P.k2 = p.k2;
+  P.V = a.V;
+  P.cpad = a.cpad;
+  P.n_pb = a.n_pb;
+  P.K_top = a.K;
+  P.rows = a.rows;
+  P.idx_sorted = a.idx_sorted;
+  P.p_sorted = a.p_sorted;
+  P.boff = a.boff;
+  P.part_m = a.part_m;
+  P.part_l = a.part_l;
+  P.part_ps = a.part_ps;
+  P.u = p.u;
+  P.ldg = a.ldg;
+  cudaError_t e = cudaMemsetAsync(p.counter, 0, sizeof(uint32_t), s);
+  if (e != cudaSuccess) return e;
+  return launch_mode<kModePass1>(P, p.num_sms, s);
+}
+
+}  // namespace kd
