@@ -154,6 +154,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", type=int, default=3)
     ap.add_argument("--chunk", type=int, default=0)
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override the token count (smaller cases for profiling)")
     ap.add_argument("--cpu-rows", type=int, default=512,
                     help="tokens in the CPU-oracle baseline sample")
     ap.add_argument("--ref-rows", type=int, default=64,
@@ -171,7 +173,7 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        x = synth.make_config(args.config)
+        x = synth.make_config(args.config, **({"N": args.tokens} if args.tokens else {}))
         run_reference(args, x)
         return
 
@@ -186,12 +188,15 @@ def main():
     torch.cuda.set_device(dev)
     kd.load_library()
 
-    x = synth.make_config(args.config)
+    c = dict(synth.CONFIGS[args.config])
+    if args.tokens:
+        c["N"] = args.tokens
+        if c.get("mask") == "packed":
+            c["mask_frac_range"] = None
     if world > 1:
         # each rank's token shard: same sizes, its own seed
-        c = dict(synth.CONFIGS[args.config])
         c["seed"] = c["seed"] + 1000 * rank
-        x = synth.make_inputs(**c)
+    x = synth.make_inputs(**c)
     N, d, V, K = x.N, x.d, x.V, x.K
     dt_code = kd.KD_BF16 if x.dtype == "bf16" else kd.KD_FP32
     chunk = args.chunk if args.chunk > 0 else kd.default_chunk(N, d, V, dt_code)

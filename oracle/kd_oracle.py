@@ -179,3 +179,29 @@ def sampled_rows(h, W, topk_idx, topk_logit, mask, T, rows, block_rows=64):
         grad_h[b0:b0 + rr.size] = G @ Wd
     return dict(rows=rows, valid=valid_all[rows], lse=lse, loss_rows=loss_rows,
                 grad_h=grad_h, n_valid=n_valid, flags=flags)
+
+
+def grad_W_rows(h, W, topk_idx, topk_logit, mask, T, vocab_rows, lse):
+    """Rows v of grad_W = (dL/dz)^T h, each computed on its own.
+
+    Column v of dL/dz needs z_rv = h_r . W_v for every token r and the
+    per-token lse (from fwd), so one grad_W row costs O(N d) once lse is
+    known.  lse is the oracle's own (NaN for rows that are not valid)."""
+    H = _f64(h)
+    Wd = _f64(W)
+    V = Wd.shape[0]
+    p, valid, _ = teacher_distribution(topk_idx, topk_logit, mask, V, T)
+    n_valid = int(valid.sum())
+    idx = np.asarray(topk_idx, dtype=np.int64)
+    in_range = (idx >= 0) & (idx < V)
+    Hv = np.where(valid[:, None], H, 0.0)
+    lse_v = np.where(valid, lse, 0.0)
+    vocab_rows = np.asarray(vocab_rows, dtype=np.int64)
+    S = (Hv @ Wd[vocab_rows].T) / T                       # [N, n]
+    G = np.exp(S - lse_v[:, None])
+    for j, v in enumerate(vocab_rows):
+        hit = in_range & (idx == v)
+        G[:, j] -= (p * hit).sum(axis=1)
+    G /= (T * max(n_valid, 1))
+    G[~valid] = 0.0
+    return G.T @ Hv

@@ -321,6 +321,15 @@ def test_sampled_rows_agree_with_dense():
     np.testing.assert_allclose(s["grad_h"], a["grad_h"][rows], rtol=1e-12, atol=1e-18)
 
 
+def test_grad_W_rows_agree_with_dense():
+    x = synth.make_inputs(50, 12, 60, 5, T=1.5, dtype="bf16", seed=21, mask="random0.2")
+    x.idx[3, 1] = x.idx[3, 0]          # a duplicate
+    a = oracle.fwd_bwd(x.h_f32(), x.W_f32(), x.idx, x.logit, x.mask, x.T)
+    vr = np.array([0, 7, int(x.idx[0, 0]), int(x.idx[3, 0]), 59])
+    g = oracle.grad_W_rows(x.h_f32(), x.W_f32(), x.idx, x.logit, x.mask, x.T, vr, a["lse"])
+    np.testing.assert_allclose(g, a["grad_W"][vr], rtol=1e-12, atol=1e-18)
+
+
 # ------------------------------------------------------------ golden regression
 
 def test_golden_tiny_config():
