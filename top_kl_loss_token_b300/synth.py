@@ -19,7 +19,8 @@ whose masked fraction falls in mask_frac_range when one is given):
   * h ~ N(0, h_std^2), W ~ N(0, w_std^2), drawn fp32; bf16 configs round them
     to bf16 with round-to-nearest-even.
   * idx: K distinct values per row, uniform in [0, V): draw 2K candidates, keep
-    the first K distinct ones in draw order, redraw the rare row that has fewer.
+    the first K distinct ones in draw order, redraw the rare row that has fewer
+    (when 4K > V: the first K entries of a random permutation instead).
   * teacher logits: base - 2 ln k + N(0, 0.5^2) for k = 1..K, sorted descending
     (index position k pairs with the k-th largest value).  The heavy-head
     variant draws the tail l_2..l_K that way and sets l_1 = l_2 + Exp(rate 2).
@@ -96,6 +97,10 @@ def distinct_indices(rng: np.random.Generator, N: int, K: int, V: int) -> np.nda
     if K > V:
         raise ValueError("cannot draw K distinct indices from fewer than K values")
     out = np.empty((N, K), dtype=np.int32)
+    if 4 * K > V:
+        # dense case: the first K entries of a random permutation of [0, V)
+        keys = rng.random((N, V))
+        return np.argsort(keys, axis=1)[:, :K].astype(np.int32)
     todo = np.arange(N)
     while todo.size:
         n = todo.size
