@@ -66,6 +66,8 @@ struct KParams {
   CUtensorMap tmB[2];
   int a_mn[2], b_mn[2];
   int M[2], N[2], K[2];
+  int bn[2];             // output tile width of the problem (multiple of 16, <= 256)
+  uint32_t tx_bytes[2];  // bytes one pipeline stage receives
   float* out[2];
   int64_t ldo[2];
   int vec_ok[2];
@@ -97,7 +99,7 @@ struct KParams {
 };
 
 struct Sizes {
-  int M[2], N[2], nkb[2], mt[2], nt[2], tiles[2];
+  int M[2], N[2], nkb[2], mt[2], nt[2], tiles[2], bn[2];
   int total;
   int count;
 };
@@ -120,7 +122,8 @@ __device__ __forceinline__ Sizes get_sizes(const KParams& P) {
     s.N[pi] = N;
     s.nkb[pi] = (K + kBK - 1) / kBK;
     s.mt[pi] = (M + kBM - 1) / kBM;
-    s.nt[pi] = (N + kBN - 1) / kBN;
+    s.bn[pi] = P.bn[pi];
+    s.nt[pi] = s.bn[pi] > 0 ? (N + s.bn[pi] - 1) / s.bn[pi] : 0;
     int tiles = s.mt[pi] * s.nt[pi];
     if (pi >= P.nprob) tiles = 0;
     // Nothing to add: an accumulating problem with an empty reduction.
@@ -209,7 +212,7 @@ __device__ void producer_loop(const KParams& P, const Sizes& S, uint8_t* smem, C
       uint8_t* sa = smem + stage * kStageBytes;
       uint8_t* sb = sa + kABytes;
       uint64_t* fb = &ctl->full[stage];
-      mbar_arrive_expect_tx(fb, kStageBytes);
+      mbar_arrive_expect_tx(fb, P.tx_bytes[pi]);
       const int k0 = kb * kBK;
       if (P.a_mn[pi]) {
 #pragma unroll
@@ -219,9 +222,10 @@ __device__ void producer_loop(const KParams& P, const Sizes& S, uint8_t* smem, C
       }
       if (P.b_mn[pi]) {
 #pragma unroll
-        for (int a = 0; a < kBN / 64; ++a) tma_load_2d(sb + a * kAtomBytes, mb, fb, tl.n * kBN + a * 64, k0);
+        for (int a = 0; a < (S.bn[pi] + 63) / 64; ++a)
+          tma_load_2d(sb + a * kAtomBytes, mb, fb, tl.n * S.bn[pi] + a * 64, k0);
       } else {
-        tma_load_2d(sb, mb, fb, k0, tl.n * kBN);
+        tma_load_2d(sb, mb, fb, k0, tl.n * S.bn[pi]);
       }
       issued[stage] += 1;
       if (++stage == kStages) {
@@ -265,7 +269,7 @@ __device__ void mma_loop(const KParams& P, const Sizes& S, uint8_t* smem, Ctl* c
     const uint32_t d_tmem = tmem + static_cast<uint32_t>(b * kBN);
     const int pi = tl.prob;
     const int a_mn = P.a_mn[pi], b_mn = P.b_mn[pi];
-    const uint32_t idesc = idesc_bf16_f32(kBM, kBN, a_mn, b_mn);
+    const uint32_t idesc = idesc_bf16_f32(kBM, S.bn[pi], a_mn, b_mn);
     bool ok = true;
     for (int kb = 0; kb < tl.nkb; ++kb) {
       if (!mbar_wait(&ctl->full[stage], phase, wc)) {
@@ -380,12 +384,13 @@ __device__ void epilogue_store(const KParams& P, const Sizes& S, Ctl* ctl, uint3
     if (lane == 0) mbar_arrive(&ctl->tempty[b]);
 
     const int i = tl.m * kBM + q * 32 + lane;
-    const int col0 = tl.n * kBN + half * 128;
-    if (i < S.M[pi] && col0 < S.N[pi]) {
+    const int col0 = tl.n * S.bn[pi] + half * 128;
+    const int ncols = min(S.bn[pi] - half * 128, S.N[pi] - col0);  // columns of this half
+    if (i < S.M[pi] && ncols > 0) {
       const int64_t orow =
           P.row_map[pi] != nullptr ? P.row_map[pi][P.row_map_off[pi] + i] : static_cast<int64_t>(i);
       float* dst = P.out[pi] + orow * P.ldo[pi] + col0;
-      const int nc = min(128, S.N[pi] - col0);
+      const int nc = min(128, ncols);
       const bool vec = P.vec_ok[pi] != 0;
       const bool acc = P.accumulate[pi] != 0;
       store_chunk32(dst, v0, nc, vec, acc);
@@ -603,6 +608,15 @@ cudaError_t launch_mode(const KParams& P, int grid, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// Output tile width for an N-wide output: the fewest 256-wide tiles, then
+// the narrowest multiple of 16 that still covers N with that many tiles
+// (d = 2880 -> 12 tiles of 240 instead of 11.25 tiles of 256).
+int tile_width(int64_t N) {
+  const int64_t tiles = (N + kBN - 1) / kBN;
+  const int64_t w = (N + tiles - 1) / tiles;
+  return static_cast<int>((w + 15) / 16 * 16);
+}
+
 bool encode_operand(CUtensorMap* m, const void* base, int mn, int64_t inner, int64_t outer,
                     int64_t ld, int rows_per_tile) {
   if (mn) return encode_tmap_bf16(m, base, inner, outer, ld, 64, kBK);
@@ -617,10 +631,13 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& g, cudaStream_t s) {
   for (int pi = 0; pi < g.nprob; ++pi) {
     const TcProblem& q = g.pr[pi];
     if (!encode_operand(&P.tmA[pi], q.A, q.a_mn, q.a_inner, q.a_outer, q.lda, kBM) ||
-        !encode_operand(&P.tmB[pi], q.B, q.b_mn, q.b_inner, q.b_outer, q.ldb, kBN))
+        !encode_operand(&P.tmB[pi], q.B, q.b_mn, q.b_inner, q.b_outer, q.ldb, tile_width(q.N)))
       return cudaErrorInvalidValue;
     P.a_mn[pi] = q.a_mn;
     P.b_mn[pi] = q.b_mn;
+    P.bn[pi] = tile_width(q.N);
+    P.tx_bytes[pi] = kABytes + (q.b_mn ? static_cast<uint32_t>((P.bn[pi] + 63) / 64) * kAtomBytes
+                                       : static_cast<uint32_t>(P.bn[pi]) * kBK * 2);
     P.M[pi] = static_cast<int>(q.M);
     P.N[pi] = static_cast<int>(q.N);
     P.K[pi] = static_cast<int>(q.K);
@@ -655,6 +672,8 @@ cudaError_t launch_tc_pass1(const Pass1Args& p, const ChunkArgs& a, cudaStream_t
   P.M[0] = a.chunk;
   P.N[0] = a.V;
   P.K[0] = static_cast<int>(p.d);
+  P.bn[0] = kBN;  // the epilogue's 128-column statistic blocks need full 256-wide tiles
+  P.tx_bytes[0] = kStageBytes;
   P.count_mode[0] = 1;
   P.nprob = 1;
   P.n_valid = a.n_valid;
