@@ -89,6 +89,11 @@ def test_full_size_chunk_invariance_and_token_split(kd):
     g1 = run_gpu(kd, x1, tensors=(h, W, idx, lg, torch.from_numpy(m1).cuda()))
     g2 = run_gpu(kd, x2, tensors=(h, W, idx, lg, torch.from_numpy(1 - m1).cuda()))
     comb = (g1["grad_W"] * g1["n_valid"] + g2["grad_W"] * g2["n_valid"]) / N
-    assert max_rel_err(comb, a["grad_W"]) <= 2e-3
+    # Unlike the chunk change above, the split changes N_valid, so each run
+    # scales its bf16 gradient tile by a different 1/(T N_valid) and rounds it
+    # on its own: the stored exponentials (rel. 2^-9 on q) and the tile itself
+    # (rel. 2^-9 on G) carry up to 2^-9 (|q| + |G|) each, so two runs may
+    # differ by about 4 * 2^-9 = 7.8e-3 of the largest entry.
+    assert max_rel_err(comb, a["grad_W"]) <= 4 * 2.0 ** -9
     lcomb = (g1["loss"] * g1["n_valid"] + g2["loss"] * g2["n_valid"]) / N
     assert lcomb == pytest.approx(a["loss"], rel=1e-5)
