@@ -128,6 +128,46 @@ kd_status kd_topk_kl_fwd(const void* h, const void* W, kd_dtype dtype, const int
                          void* workspace, size_t ws_bytes, uint32_t* dev_err_flags,
                          cudaStream_t stream);
 
+/*
+ * kd_topk_kl_fwd_bwd_noalloc -- kd_topk_kl_fwd_bwd for callers that cannot
+ * allocate device memory.  (The write-ups have no counterpart: this is an
+ * interface convenience, not part of the method.)
+ *
+ * Who needs it: code that may not call cudaMalloc -- a region being captured
+ * into a CUDA graph, a process whose memory pool owns the device and forbids
+ * allocations beside it, a plug-in that is handed device pointers for its
+ * inputs and outputs but no allocator -- still has to supply the workspace
+ * that kd_topk_kl_fwd_bwd takes.  This call uses instead a scratch array of
+ * KD_NOALLOC_SCRATCH_BYTES that the library holds in device memory: every GPU
+ * that loads the library keeps that array until the process exits.  The call
+ * itself allocates nothing (no cudaMalloc, cudaFree or allocating library
+ * routine).
+ *
+ * Arguments, results, device error flags and host-side errors are those of
+ * kd_topk_kl_fwd_bwd, without the workspace.  chunk <= 0 picks the largest
+ * chunk (a multiple of 128 tokens, at most kd_topk_kl_default_chunk) whose
+ * workspace fits in the array; a request whose workspace
+ * (kd_topk_kl_workspace_bytes) exceeds KD_NOALLOC_SCRATCH_BYTES even at that
+ * smallest chunk, or at the chunk the caller passed, returns KD_ERR_WORKSPACE
+ * before any CUDA call.
+ *
+ * Set-up: the first call on a device, with that device current, looks up the
+ * array's device address (cudaGetSymbolAddress, which may load the library's
+ * device code); make that first call before any stream capture.  Every call
+ * on a device shares the one array, and the array keeps the previous call's
+ * contents (each call clears the parts that must start at zero).  Calls that
+ * overlap on the GPU -- on different streams, or from different host threads
+ * -- race on the array and give wrong results: order them on one stream.
+ */
+#define KD_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+kd_status kd_topk_kl_fwd_bwd_noalloc(const void* h, const void* W, kd_dtype dtype,
+                                     const int32_t* topk_idx, const float* topk_logit,
+                                     const uint8_t* mask, int64_t N, int64_t d, int64_t V,
+                                     int32_t K, float T, int64_t chunk, float* loss,
+                                     float* grad_h, float* grad_W, uint32_t* dev_err_flags,
+                                     cudaStream_t stream);
+
 /* A static, human-readable name for a status code. */
 const char* kd_status_string(kd_status status);
 

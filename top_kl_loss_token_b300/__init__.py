@@ -34,7 +34,11 @@ STATUS = {0: "KD_OK", 1: "KD_ERR_INVALID_ARG", 2: "KD_ERR_UNSUPPORTED", 3: "KD_E
 # Every symbol the headers declare.
 EXPORTS = ["kd_topk_kl_workspace_bytes", "kd_topk_kl_default_chunk", "kd_topk_kl_fwd_bwd",
            "kd_topk_kl_fwd", "kd_status_string", "kd_topk_kl_workspace_layout",
-           "kd_umma_gemm_bf16", "kd_timing_enable", "kd_timing_collect"]
+           "kd_umma_gemm_bf16", "kd_timing_enable", "kd_timing_collect",
+           "kd_topk_kl_fwd_bwd_noalloc"]
+
+# Size of the library-held scratch array used by kd_topk_kl_fwd_bwd_noalloc.
+KD_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 _LIB = None
 
@@ -81,6 +85,9 @@ def load_library(path: str = LIB_PATH):
     lib.kd_topk_kl_fwd.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, i64, i64, i64, i32, f32, i64,
                                    vp, vp, sz, vp, vp]
     lib.kd_topk_kl_fwd.restype = ctypes.c_int
+    lib.kd_topk_kl_fwd_bwd_noalloc.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, i64, i64, i64,
+                                               i32, f32, i64, vp, vp, vp, vp, vp]
+    lib.kd_topk_kl_fwd_bwd_noalloc.restype = ctypes.c_int
     lib.kd_status_string.argtypes = [ctypes.c_int]
     lib.kd_status_string.restype = ctypes.c_char_p
     lib.kd_umma_gemm_bf16.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.c_int, ctypes.c_int,
@@ -209,6 +216,27 @@ def kd_topk_kl_fwd(h, W, topk_idx, topk_logit, mask=None, T: float = 1.0, chunk:
     return loss, workspace
 
 
+def kd_topk_kl_fwd_bwd_noalloc(h, W, topk_idx, topk_logit, loss, grad_h, grad_W, mask=None,
+                               T: float = 1.0, chunk: int = 0, err_flags=None, stream=None):
+    """kd_topk_kl_fwd_bwd for callers that cannot allocate device memory (see
+    include/kd_topk_kl.h): the workspace is the library's own fixed scratch
+    array, and the caller passes the output tensors, so this function
+    allocates nothing on the device.  Returns (loss, grad_h, grad_W)."""
+    N, d, V, K = _validate(h, W, topk_idx, topk_logit, mask)
+    dt = _dtype_code(h)
+    for name, t, shape in (("loss", loss, (1,)), ("grad_h", grad_h, (N, d)),
+                           ("grad_W", grad_W, (V, d))):
+        if (not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != shape
+                or t.element_size() != 4 or not t.is_floating_point()):
+            raise ValueError(f"{name} must be a contiguous fp32 CUDA tensor of shape {shape}")
+    st = load_library().kd_topk_kl_fwd_bwd_noalloc(
+        _ptr(h), _ptr(W), dt, _ptr(topk_idx), _ptr(topk_logit), _ptr(mask), N, d, V, K,
+        float(T), int(chunk), _ptr(loss), _ptr(grad_h), _ptr(grad_W), _ptr(err_flags),
+        _stream_handle(stream))
+    _check(st, "kd_topk_kl_fwd_bwd_noalloc")
+    return loss, grad_h, grad_W
+
+
 def kd_umma_gemm_bf16(A, B, M: int, N: int, K: int, a_mn_major: bool, b_mn_major: bool,
                       out=None, accumulate: bool = False, err_flags=None, stream=None):
     """D[M, N] (+)= A(m, k) B(n, k) on the tensor cores (see kd_topk_kl_steps.h)."""
@@ -257,5 +285,6 @@ def workspace_view(workspace, lay: WorkspaceLayout, name: str, count: int, dtype
 # Short names.
 fwd_bwd = kd_topk_kl_fwd_bwd
 fwd = kd_topk_kl_fwd
+fwd_bwd_noalloc = kd_topk_kl_fwd_bwd_noalloc
 timing_enable = kd_timing_enable
 timing_collect = kd_timing_collect
