@@ -12,13 +12,12 @@
 
 namespace kd {
 
-// Tensor-core tiles: one CTA owns a 128 x 256 fp32 accumulator in TMEM (two of
-// them, double-buffered) and streams 64-deep K blocks of both operands
-// through a 4-stage shared-memory ring.
+// Tensor-core tiles: a CTA pair owns a 256 x 256 output tile; each CTA holds
+// its 128 rows x 256 fp32 columns in TMEM (two of them, double-buffered) and
+// streams 64-deep K blocks of its halves of both operands.
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
-constexpr int kStages = 4;
 // The logsumexp statistics are kept per 128-column block of the vocabulary.
 constexpr int kPB = 128;
 // A sorted-index slot that holds no entry (dropped, or padding).

@@ -15,17 +15,30 @@
 //            grad_W (+)= G_c^T h_c              (M = V, N = d, K = chunk),
 //            both in the same launch, fp32 results stored or accumulated.
 //
-// CTA layout (320 threads, one CTA per SM):
-//   warp 0      TMA producer: takes tile numbers from a global counter, hands
-//               them to the other roles through a shared-memory ring, and
-//               streams 64-deep K blocks of A and B into a 4-stage ring;
-//   warp 1      allocates TMEM (two 128 x 256 fp32 accumulators) and issues
-//               tcgen05.mma (128 x 256 x 16, bf16 in, fp32 out) from one lane;
-//   warps 2-9   epilogue: each warp reads 32 TMEM lanes (rows) x 128 columns.
+// The kernel runs as clusters of two CTAs ("CTA pairs", one CTA per SM).  A
+// pair owns a 256-row output tile: each CTA stages its 128 rows of A and half
+// of the tile's B columns, and one tcgen05.mma.cta_group::2 issued by the
+// pair's first CTA multiplies the whole 256 x N tile, each CTA's tensor
+// memory receiving its own 128 rows.  Staging half of B per SM halves the
+// operand bytes per stage, so 7 stages of 64-deep K blocks fit in shared
+// memory.
+//
+// CTA layout (320 threads):
+//   warp 0      TMA producer.  In the first CTA it takes tile numbers from a
+//               global counter and hands them to every role of both CTAs
+//               through a shared-memory ring; both CTAs' producers stream
+//               their halves of each K block into a 7-stage ring whose
+//               "full" barrier lives in the first CTA;
+//   warp 1      allocates TMEM for the pair (two 128 x 256 fp32 accumulators
+//               per CTA); in the first CTA one lane issues the pair MMAs
+//               (256 x N x 16, bf16 in, fp32 out);
+//   warps 2-9   epilogue: each warp reads 32 TMEM lanes (rows) x 128 columns
+//               of its own CTA's accumulator.
 // Operands are staged in the 128-byte swizzle layout; a K-major operand tile
 // is one TMA box of 64 x rows, an MN-major tile is made of 64 x 64 boxes.
 // Every wait is time-bounded (kd_ptx.cuh): on a timeout the CTA records
-// KD_FLAG_TIMEOUT, drains its in-flight copies and MMAs, frees TMEM and exits.
+// KD_FLAG_TIMEOUT, tells the other CTA of the pair, drains its in-flight
+// copies and MMAs, frees TMEM and exits.
 #include <math.h>
 #include <string.h>
 
@@ -38,19 +51,23 @@ namespace {
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr int kSched = 4;
+constexpr int kStages = 7;
+constexpr int kPairM = 2 * kBM;                 // rows of a pair's output tile
 constexpr uint32_t kTmemCols = 2 * kBN;
-constexpr int kABytes = kBM * kBK * 2;
-constexpr int kBBytes = kBN * kBK * 2;
+constexpr int kABytes = kBM * kBK * 2;          // this CTA's 128 rows of A
+constexpr int kBBytes = (kBN / 2) * kBK * 2;    // this CTA's half of B (at most)
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kAtomBytes = 64 * kBK * 2;  // one 64 (MN) x 64 (K) box of an MN-major tile
 
+// Barriers and the tile ring.  In the pair's second CTA, full[], tempty[] and
+// sempty[] are unused: those waits happen in the first CTA.
 struct Ctl {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
-  uint64_t tfull[2];
-  uint64_t tempty[2];
-  uint64_t sfull[kSched];
-  uint64_t sempty[kSched];
+  uint64_t full[kStages];   // first CTA: both CTAs' operands of a stage landed
+  uint64_t empty[kStages];  // each CTA: the pair MMAs reading a stage are done
+  uint64_t tfull[2];        // each CTA: accumulator b is complete
+  uint64_t tempty[2];       // first CTA: both CTAs' epilogues have read accumulator b
+  uint64_t sfull[kSched];   // each CTA: a tile number is in sched_tile[slot]
+  uint64_t sempty[kSched];  // first CTA: every role of both CTAs has taken it
   uint64_t drain;
   int sched_tile[kSched];
   uint32_t tmem_base;
@@ -58,6 +75,11 @@ struct Ctl {
 };
 
 constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStages) * kStageBytes + sizeof(Ctl);
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+
+// Arrivals that complete one phase of the first CTA's barriers.
+constexpr uint32_t kTemptyCount = 2 * kEpiWarps;          // epilogue warps of both CTAs
+constexpr uint32_t kSemptyCount = 1 + kEpiWarps + 1 + kEpiWarps;  // MMA + epi, peer producer + epi
 
 enum : int { kModePass1 = 0, kModeStore = 1 };
 
@@ -67,7 +89,7 @@ struct KParams {
   int a_mn[2], b_mn[2];
   int M[2], N[2], K[2];
   int bn[2];             // output tile width of the problem (multiple of 16, <= 256)
-  uint32_t tx_bytes[2];  // bytes one pipeline stage receives
+  uint32_t tx_bytes[2];  // bytes one pipeline stage receives in both CTAs together
   float* out[2];
   int64_t ldo[2];
   int vec_ok[2];
@@ -121,7 +143,7 @@ __device__ __forceinline__ Sizes get_sizes(const KParams& P) {
     s.M[pi] = M;
     s.N[pi] = N;
     s.nkb[pi] = (K + kBK - 1) / kBK;
-    s.mt[pi] = (M + kBM - 1) / kBM;
+    s.mt[pi] = (M + kPairM - 1) / kPairM;
     s.bn[pi] = P.bn[pi];
     s.nt[pi] = s.bn[pi] > 0 ? (N + s.bn[pi] - 1) / s.bn[pi] : 0;
     int tiles = s.mt[pi] * s.nt[pi];
@@ -175,9 +197,26 @@ __device__ __forceinline__ bool sched_pop(Ctl* ctl, int& slot, uint32_t& sphase,
   return true;
 }
 
+// Hands the next tile number to the consumers of ring slot `slot` (first
+// CTA's producer only): writes it into both CTAs' rings and arrives on both
+// CTAs' "full" barriers of that slot.
+__device__ __forceinline__ void sched_push(Ctl* ctl, int slot, int t) {
+  const uint32_t tile_local = smem_u32(&ctl->sched_tile[slot]);
+  const uint32_t bar_local = smem_u32(&ctl->sfull[slot]);
+  st_cluster_u32(mapa_shared(tile_local, 0), static_cast<uint32_t>(t));
+  st_cluster_u32(mapa_shared(tile_local, 1), static_cast<uint32_t>(t));
+  mbar_arrive_cluster(mapa_shared(bar_local, 0));
+  mbar_arrive_cluster(mapa_shared(bar_local, 1));
+}
+
+// Tells the first CTA that this role has taken ring slot `slot`.
+__device__ __forceinline__ void sched_release(Ctl* ctl, int slot) {
+  mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->sempty[slot]), 0));
+}
+
 template <int MODE>
 __device__ void producer_loop(const KParams& P, const Sizes& S, uint8_t* smem, Ctl* ctl,
-                              const WaitCtx& wc) {
+                              const WaitCtx& wc, uint32_t rank) {
   int stage = 0;
   uint32_t phase = 0;
   int slot = 0;
@@ -186,15 +225,24 @@ __device__ void producer_loop(const KParams& P, const Sizes& S, uint8_t* smem, C
 #pragma unroll
   for (int s = 0; s < kStages; ++s) issued[s] = 0;
   bool aborted = false;
+  const bool leader = rank == 0;
   while (true) {
-    if (!mbar_wait(&ctl->sempty[slot], sphase ^ 1u, wc)) {
-      aborted = true;
-      break;
+    int t;
+    if (leader) {
+      if (!mbar_wait(&ctl->sempty[slot], sphase ^ 1u, wc)) {
+        aborted = true;
+        break;
+      }
+      t = static_cast<int>(atomicAdd(P.counter, 1u));
+      if (t >= S.total) t = -1;
+      sched_push(ctl, slot, t);
+    } else {
+      if (!sched_pop(ctl, slot, sphase, t, wc)) {
+        aborted = true;
+        break;
+      }
+      sched_release(ctl, slot);
     }
-    int t = static_cast<int>(atomicAdd(P.counter, 1u));
-    if (t >= S.total) t = -1;
-    *reinterpret_cast<volatile int*>(&ctl->sched_tile[slot]) = t;
-    mbar_arrive(&ctl->sfull[slot]);
     if (++slot == kSched) {
       slot = 0;
       sphase ^= 1u;
@@ -204,6 +252,9 @@ __device__ void producer_loop(const KParams& P, const Sizes& S, uint8_t* smem, C
     const int pi = tl.prob;
     const CUtensorMap* ma = &P.tmA[pi];
     const CUtensorMap* mb = &P.tmB[pi];
+    const int bn_half = S.bn[pi] >> 1;
+    const int a_row0 = tl.m * kPairM + static_cast<int>(rank) * kBM;
+    const int b_col0 = tl.n * S.bn[pi] + static_cast<int>(rank) * bn_half;
     for (int kb = 0; kb < tl.nkb; ++kb) {
       if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, wc)) {
         aborted = true;
@@ -211,21 +262,23 @@ __device__ void producer_loop(const KParams& P, const Sizes& S, uint8_t* smem, C
       }
       uint8_t* sa = smem + stage * kStageBytes;
       uint8_t* sb = sa + kABytes;
-      uint64_t* fb = &ctl->full[stage];
-      mbar_arrive_expect_tx(fb, P.tx_bytes[pi]);
+      // Both CTAs' copies complete on the first CTA's barrier, which expects
+      // the bytes of both.
+      if (leader) mbar_arrive_expect_tx(&ctl->full[stage], P.tx_bytes[pi]);
+      const uint32_t fb = mapa_shared(smem_u32(&ctl->full[stage]), 0);
       const int k0 = kb * kBK;
       if (P.a_mn[pi]) {
 #pragma unroll
-        for (int a = 0; a < kBM / 64; ++a) tma_load_2d(sa + a * kAtomBytes, ma, fb, tl.m * kBM + a * 64, k0);
+        for (int a = 0; a < kBM / 64; ++a)
+          tma_load_2d_pair(sa + a * kAtomBytes, ma, fb, a_row0 + a * 64, k0);
       } else {
-        tma_load_2d(sa, ma, fb, k0, tl.m * kBM);
+        tma_load_2d_pair(sa, ma, fb, k0, a_row0);
       }
       if (P.b_mn[pi]) {
-#pragma unroll
-        for (int a = 0; a < (S.bn[pi] + 63) / 64; ++a)
-          tma_load_2d(sb + a * kAtomBytes, mb, fb, tl.n * S.bn[pi] + a * 64, k0);
+        for (int a = 0; a < (bn_half + 63) / 64; ++a)
+          tma_load_2d_pair(sb + a * kAtomBytes, mb, fb, b_col0 + a * 64, k0);
       } else {
-        tma_load_2d(sb, mb, fb, k0, tl.n * S.bn[pi]);
+        tma_load_2d_pair(sb, mb, fb, k0, b_col0);
       }
       issued[stage] += 1;
       if (++stage == kStages) {
@@ -236,13 +289,23 @@ __device__ void producer_loop(const KParams& P, const Sizes& S, uint8_t* smem, C
     if (aborted) break;
   }
   if (aborted) {
-    // Let the copies already issued land before the CTA's shared memory goes away.
+    // Let the copies already issued land before the CTA's shared memory goes
+    // away.  Their completion is counted in the first CTA only, so the second
+    // CTA just waits a fixed 20 ms (a copy takes microseconds).
+    if (leader) {
 #pragma unroll
-    for (int s = 0; s < kStages; ++s)
-      if (issued[s] != 0) mbar_wait_drain(&ctl->full[s], (issued[s] - 1u) & 1u, P.err);
+      for (int s = 0; s < kStages; ++s)
+        if (issued[s] != 0)
+          mbar_wait_drain(&ctl->full[s], (issued[s] - 1u) & 1u, P.err, 20000000ull);
+    } else {
+      const uint64_t t0 = globaltimer_ns();
+      while (globaltimer_ns() - t0 < 20000000ull) {
+      }
+    }
   }
 }
 
+// Pair MMA issue (first CTA, one thread).
 template <int MODE>
 __device__ void mma_loop(const KParams& P, const Sizes& S, uint8_t* smem, Ctl* ctl, uint32_t tmem,
                          const WaitCtx& wc) {
@@ -254,7 +317,7 @@ __device__ void mma_loop(const KParams& P, const Sizes& S, uint8_t* smem, Ctl* c
   while (true) {
     int t;
     if (!sched_pop(ctl, slot, sphase, t, wc)) break;
-    mbar_arrive(&ctl->sempty[slot]);
+    sched_release(ctl, slot);
     if (++slot == kSched) {
       slot = 0;
       sphase ^= 1u;
@@ -269,7 +332,7 @@ __device__ void mma_loop(const KParams& P, const Sizes& S, uint8_t* smem, Ctl* c
     const uint32_t d_tmem = tmem + static_cast<uint32_t>(b * kBN);
     const int pi = tl.prob;
     const int a_mn = P.a_mn[pi], b_mn = P.b_mn[pi];
-    const uint32_t idesc = idesc_bf16_f32(kBM, S.bn[pi], a_mn, b_mn);
+    const uint32_t idesc = idesc_bf16_f32(kPairM, S.bn[pi], a_mn, b_mn);
     bool ok = true;
     for (int kb = 0; kb < tl.nkb; ++kb) {
       if (!mbar_wait(&ctl->full[stage], phase, wc)) {
@@ -287,19 +350,19 @@ __device__ void mma_loop(const KParams& P, const Sizes& S, uint8_t* smem, Ctl* c
                                  : sdesc_sw128(sa + kk * 32, 16, 1024);
         const uint64_t bd = b_mn ? sdesc_sw128(sb + kk * 2048, kAtomBytes, 1024)
                                  : sdesc_sw128(sb + kk * 32, 16, 1024);
-        umma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+        umma_bf16_pair(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
       }
-      umma_commit(&ctl->empty[stage]);
+      umma_commit_pair_both(&ctl->empty[stage]);
       if (++stage == kStages) {
         stage = 0;
         phase ^= 1u;
       }
     }
     if (!ok) break;
-    umma_commit(&ctl->tfull[b]);
+    umma_commit_pair_both(&ctl->tfull[b]);
   }
   // Every MMA this thread issued must finish before TMEM is freed.
-  umma_commit(&ctl->drain);
+  umma_commit_pair_local(&ctl->drain);
   mbar_wait_drain(&ctl->drain, 0, P.err);
 }
 
@@ -343,7 +406,7 @@ __device__ __forceinline__ void store_chunk32(float* dst, const float (&v)[32], 
 }
 
 __device__ void epilogue_store(const KParams& P, const Sizes& S, Ctl* ctl, uint32_t tmem,
-                               const WaitCtx& wc, int warp, int lane) {
+                               const WaitCtx& wc, int warp, int lane, int rank) {
   const int q = warp & 3;           // TMEM lane quarter this warp may read
   const int half = (warp - 2) >> 2; // which 128 columns of the 256
   int slot = 0;
@@ -355,7 +418,7 @@ __device__ void epilogue_store(const KParams& P, const Sizes& S, Ctl* ctl, uint3
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) break;
     __syncwarp();
-    if (lane == 0) mbar_arrive(&ctl->sempty[slot]);
+    if (lane == 0) sched_release(ctl, slot);
     if (++slot == kSched) {
       slot = 0;
       sphase ^= 1u;
@@ -381,9 +444,9 @@ __device__ void epilogue_store(const KParams& P, const Sizes& S, Ctl* ctl, uint3
     }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&ctl->tempty[b]);
+    if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->tempty[b]), 0));
 
-    const int i = tl.m * kBM + q * 32 + lane;
+    const int i = tl.m * kPairM + rank * kBM + q * 32 + lane;
     const int col0 = tl.n * S.bn[pi] + half * 128;
     const int ncols = min(S.bn[pi] - half * 128, S.N[pi] - col0);  // columns of this half
     if (i < S.M[pi] && ncols > 0) {
@@ -433,7 +496,7 @@ __device__ __forceinline__ float max32(const float (&v)[32], int nvalid, bool ma
 }
 
 __device__ void epilogue_pass1(const KParams& P, const Sizes& S, Ctl* ctl, uint32_t tmem,
-                               const WaitCtx& wc, int warp, int lane) {
+                               const WaitCtx& wc, int warp, int lane, int rank) {
   const int q = warp & 3;
   const int half = (warp - 2) >> 2;
   int slot = 0;
@@ -446,7 +509,7 @@ __device__ void epilogue_pass1(const KParams& P, const Sizes& S, Ctl* ctl, uint3
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) break;
     __syncwarp();
-    if (lane == 0) mbar_arrive(&ctl->sempty[slot]);
+    if (lane == 0) sched_release(ctl, slot);
     if (++slot == kSched) {
       slot = 0;
       sphase ^= 1u;
@@ -457,7 +520,7 @@ __device__ void epilogue_pass1(const KParams& P, const Sizes& S, Ctl* ctl, uint3
     const uint32_t tp = (static_cast<uint32_t>(it) >> 1) & 1u;
     ++it;
 
-    const int i = tl.m * kBM + q * 32 + lane;  // row within the chunk
+    const int i = tl.m * kPairM + rank * kBM + q * 32 + lane;  // row within the chunk
     const int col0 = tl.n * kBN + half * 128;  // first vocabulary column of this block
     const int pb = tl.n * 2 + half;            // 128-column block index
     const bool live = (i < S.count) && (pb < P.n_pb);
@@ -502,7 +565,7 @@ __device__ void epilogue_pass1(const KParams& P, const Sizes& S, Ctl* ctl, uint3
     }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&ctl->tempty[b]);
+    if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->tempty[b]), 0));
 
     if (live) {
       const int nv = min(128, P.V - col0);
@@ -541,6 +604,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + kStages * kStageBytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  // Both CTAs of a pair see the same sizes, so both leave here or neither.
   const Sizes S = get_sizes(P);
   if (S.total == 0) return;
 
@@ -553,12 +618,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
 #pragma unroll
     for (int b = 0; b < 2; ++b) {
       mbar_init(&ctl->tfull[b], 1);
-      mbar_init(&ctl->tempty[b], kEpiWarps);
+      mbar_init(&ctl->tempty[b], kTemptyCount);
     }
 #pragma unroll
     for (int s = 0; s < kSched; ++s) {
       mbar_init(&ctl->sfull[s], 1);
-      mbar_init(&ctl->sempty[s], 1 + kEpiWarps);
+      mbar_init(&ctl->sempty[s], kSemptyCount);
     }
     mbar_init(&ctl->drain, 1);
     ctl->abort = 0;
@@ -572,40 +637,67 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       tma_prefetch_desc(&P.tmB[1]);
     }
   }
-  if (warp == 1) tmem_alloc(&ctl->tmem_base, kTmemCols);
+  // Both CTAs' barriers are initialised before either CTA arrives on the
+  // other's, and the other CTA is running before the pair allocates TMEM.
+  cluster_sync_all();
+  if (warp == 1) tmem_alloc_pair(&ctl->tmem_base, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
-  const WaitCtx wc{&ctl->abort, P.err};
+  const WaitCtx wc{&ctl->abort, mapa_shared(smem_u32(&ctl->abort), rank ^ 1u), P.err};
 
   if (warp == 0) {
-    if (lane == 0) producer_loop<MODE>(P, S, smem, ctl, wc);
+    if (lane == 0) producer_loop<MODE>(P, S, smem, ctl, wc, rank);
   } else if (warp == 1) {
-    if (lane == 0) mma_loop<MODE>(P, S, smem, ctl, tmem, wc);
+    if (lane == 0 && rank == 0) mma_loop<MODE>(P, S, smem, ctl, tmem, wc);
   } else {
     if (MODE == kModePass1)
-      epilogue_pass1(P, S, ctl, tmem, wc, warp, lane);
+      epilogue_pass1(P, S, ctl, tmem, wc, warp, lane, static_cast<int>(rank));
     else
-      epilogue_store(P, S, ctl, tmem, wc, warp, lane);
+      epilogue_store(P, S, ctl, tmem, wc, warp, lane, static_cast<int>(rank));
   }
 
+  // No CTA leaves while the other may still arrive on its barriers or have
+  // pair MMAs read its shared memory; then the pair frees its TMEM together.
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc_pair(tmem, kTmemCols);
   }
 }
 
 template <int MODE>
-cudaError_t launch_mode(const KParams& P, int grid, cudaStream_t s) {
+cudaError_t launch_mode(const KParams& P, int num_sms, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<MODE>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
-  tc_gemm_kernel<MODE><<<grid, kThreads, kSmemBytes, s>>>(P);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // One pair per two SMs, as many as can be resident together (persistent).
+  int pairs = num_sms / 2;
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  int fit = 0;
+  if (cudaOccupancyMaxActiveClusters(&fit, tc_gemm_kernel<MODE>, &cfg) == cudaSuccess && fit > 0 &&
+      fit < pairs)
+    pairs = fit;
+  cudaGetLastError();
+  if (pairs < 1) pairs = 1;
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<MODE>, P);
 }
 
 // Output tile width for an N-wide output: the fewest 256-wide tiles, then
@@ -630,14 +722,17 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& g, cudaStream_t s) {
   memset(&P, 0, sizeof(P));
   for (int pi = 0; pi < g.nprob; ++pi) {
     const TcProblem& q = g.pr[pi];
+    const int bn = tile_width(q.N);
     if (!encode_operand(&P.tmA[pi], q.A, q.a_mn, q.a_inner, q.a_outer, q.lda, kBM) ||
-        !encode_operand(&P.tmB[pi], q.B, q.b_mn, q.b_inner, q.b_outer, q.ldb, tile_width(q.N)))
+        !encode_operand(&P.tmB[pi], q.B, q.b_mn, q.b_inner, q.b_outer, q.ldb, bn / 2))
       return cudaErrorInvalidValue;
     P.a_mn[pi] = q.a_mn;
     P.b_mn[pi] = q.b_mn;
-    P.bn[pi] = tile_width(q.N);
-    P.tx_bytes[pi] = kABytes + (q.b_mn ? static_cast<uint32_t>((P.bn[pi] + 63) / 64) * kAtomBytes
-                                       : static_cast<uint32_t>(P.bn[pi]) * kBK * 2);
+    P.bn[pi] = bn;
+    // each CTA: its 128 rows of A and its bn/2 columns of B
+    const uint32_t b_bytes = q.b_mn ? static_cast<uint32_t>((bn / 2 + 63) / 64) * kAtomBytes
+                                    : static_cast<uint32_t>(bn / 2) * kBK * 2;
+    P.tx_bytes[pi] = 2u * (kABytes + b_bytes);
     P.M[pi] = static_cast<int>(q.M);
     P.N[pi] = static_cast<int>(q.N);
     P.K[pi] = static_cast<int>(q.K);
@@ -665,7 +760,7 @@ cudaError_t launch_tc_pass1(const Pass1Args& p, const ChunkArgs& a, cudaStream_t
   KParams P;
   memset(&P, 0, sizeof(P));
   if (!encode_operand(&P.tmA[0], p.hc, 0, p.d, a.cpad, p.d, kBM) ||
-      !encode_operand(&P.tmB[0], p.W, 0, p.d, a.V, p.d, kBN))
+      !encode_operand(&P.tmB[0], p.W, 0, p.d, a.V, p.d, kBN / 2))
     return cudaErrorInvalidValue;
   P.tmA[1] = P.tmA[0];
   P.tmB[1] = P.tmB[0];
@@ -673,7 +768,7 @@ cudaError_t launch_tc_pass1(const Pass1Args& p, const ChunkArgs& a, cudaStream_t
   P.N[0] = a.V;
   P.K[0] = static_cast<int>(p.d);
   P.bn[0] = kBN;  // the epilogue's 128-column statistic blocks need full 256-wide tiles
-  P.tx_bytes[0] = kStageBytes;
+  P.tx_bytes[0] = 2u * kStageBytes;
   P.count_mode[0] = 1;
   P.nprob = 1;
   P.n_valid = a.n_valid;
