@@ -124,6 +124,20 @@ bool encode_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_tmap_bf16_mn3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                           uint64_t ld_elems, uint32_t atoms, uint32_t box_k) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr || inner % 64 != 0) return false;
+  // [inner / 64][outer][64]: element (mn, k) at mn % 64 + k * ld + (mn / 64) * 64
+  const cuuint64_t dims[3] = {64, outer, inner / 64};
+  const cuuint64_t strides[2] = {ld_elems * 2, 128};
+  const cuuint32_t box[3] = {64, box_k, atoms};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int64_t default_chunk(int64_t N, int64_t d, int64_t V, kd_dtype dtype) {
   (void)d;
   const int64_t elem = dtype == KD_BF16 ? 2 : 4;
@@ -360,7 +374,8 @@ kd_status run(const void* h, const void* W, kd_dtype dtype, const int32_t* topk_
       TcProblem& gw = g.pr[1];  // grad_W (+)= G_c^T h_c
       gw.A = v.g;
       gw.a_mn = 1;
-      gw.a_inner = V;
+      // G's columns V .. ldg are zero, so whole 64-column atoms may be read
+      gw.a_inner = round_up(V, 64);
       gw.a_outer = P.cpad;
       gw.lda = P.ldg;
       gw.B = v.hc;

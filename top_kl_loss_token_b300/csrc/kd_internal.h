@@ -111,6 +111,13 @@ cudaError_t launch_simt_gemm(const SimtGemm& g, cudaStream_t s);
 bool encode_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                       uint64_t ld_elems, uint32_t box_inner, uint32_t box_outer);
 
+// An MN-major bf16 operand stored [outer = K][inner = MN] (MN contiguous,
+// inner a multiple of 64), viewed as [inner / 64][outer][64] so that one box
+// of `atoms` x box_k x 64 brings `atoms` consecutive 64-element atoms in the
+// 128-byte swizzle layout.
+bool encode_tmap_bf16_mn3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                           uint64_t ld_elems, uint32_t atoms, uint32_t box_k);
+
 struct Pass1Args {
   const void* hc;  // [cpad, d] bf16
   const void* W;   // [V, d] bf16

@@ -92,6 +92,12 @@ static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, co
   }
 }
 
+// mbar_wait with the common case (phase already complete) inlined.
+__device__ __forceinline__ bool mbar_wait_fast(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
+  if (mbar_try_wait(smem_u32(bar), parity)) return true;
+  return mbar_wait(bar, parity, w);
+}
+
 // Same, but only for draining at exit: it ignores the abort flag and just
 // bounds the time.
 static __device__ __noinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint32_t* err,
@@ -162,6 +168,18 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y)
+      : "memory");
+}
+
+// 3-D tiled load (x innermost), otherwise as tma_load_2d_pair.  Used for
+// MN-major operands whose tile spans several 64-element atoms: the tensor is
+// viewed as [MN / 64][K][64] so one box brings every atom of the tile.
+__device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* m,
+                                                 uint32_t bar_cluster, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
 

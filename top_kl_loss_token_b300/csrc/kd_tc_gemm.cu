@@ -24,18 +24,22 @@
 // memory.
 //
 // CTA layout (320 threads):
-//   warp 0      TMA producer.  In the first CTA it takes tile numbers from a
-//               global counter and hands them to every role of both CTAs
-//               through a shared-memory ring; both CTAs' producers stream
-//               their halves of each K block into a 7-stage ring whose
-//               "full" barrier lives in the first CTA;
+//   warp 0      TMA producer of A.  In the first CTA it also takes tile
+//               numbers from a global counter and hands them to every role of
+//               both CTAs through a shared-memory ring;
+//   warp 10     TMA producer of B.  Both CTAs' producers stream their halves
+//               of each K block into a 7-stage ring whose "full" barrier lives
+//               in the first CTA.  A and B are issued from separate warps
+//               because one thread issuing every tensor copy of a stage in
+//               turn cannot keep the pair's MMA fed;
 //   warp 1      allocates TMEM for the pair (two 128 x 256 fp32 accumulators
 //               per CTA); in the first CTA one lane issues the pair MMAs
 //               (256 x N x 16, bf16 in, fp32 out);
 //   warps 2-9   epilogue: each warp reads 32 TMEM lanes (rows) x 128 columns
 //               of its own CTA's accumulator.
 // Operands are staged in the 128-byte swizzle layout; a K-major operand tile
-// is one TMA box of 64 x rows, an MN-major tile is made of 64 x 64 boxes.
+// is one TMA box of 64 x rows, an MN-major tile is made of 64 x 64 atoms,
+// brought by one 3-D box when the tile starts on an atom boundary.
 // Every wait is time-bounded (kd_ptx.cuh): on a timeout the CTA records
 // KD_FLAG_TIMEOUT, tells the other CTA of the pair, drains its in-flight
 // copies and MMAs, frees TMEM and exits.
@@ -49,7 +53,8 @@ namespace kd {
 namespace {
 
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = (2 + kEpiWarps) * 32;
+constexpr int kBProducerWarp = 2 + kEpiWarps;    // warp 10
+constexpr int kThreads = (3 + kEpiWarps) * 32;
 constexpr int kSched = 4;
 constexpr int kStages = 7;
 constexpr int kPairM = 2 * kBM;                 // rows of a pair's output tile
@@ -79,7 +84,15 @@ static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 // Arrivals that complete one phase of the first CTA's barriers.
 constexpr uint32_t kTemptyCount = 2 * kEpiWarps;          // epilogue warps of both CTAs
-constexpr uint32_t kSemptyCount = 1 + kEpiWarps + 1 + kEpiWarps;  // MMA + epi, peer producer + epi
+// first CTA: MMA, epilogue warps, B producer; second CTA: A and B producers, epilogue warps
+constexpr uint32_t kSemptyCount = (1 + kEpiWarps + 1) + (2 + kEpiWarps);
+
+// How a stage of an operand is loaded.
+enum : int {
+  kLoadK = 0,     // K-major: one 2-D box of 64 (K) x rows
+  kLoadMN2d = 1,  // MN-major: one 2-D box of 64 (MN) x 64 (K) per 64-element atom
+  kLoadMN3d = 2   // MN-major, atom-aligned: one 3-D box covering every atom
+};
 
 enum : int { kModePass1 = 0, kModeStore = 1 };
 
@@ -87,6 +100,7 @@ struct KParams {
   CUtensorMap tmA[2];
   CUtensorMap tmB[2];
   int a_mn[2], b_mn[2];
+  int a_load[2], b_load[2];  // kLoadK / kLoadMN2d / kLoadMN3d
   int M[2], N[2], K[2];
   int bn[2];             // output tile width of the problem (multiple of 16, <= 256)
   uint32_t tx_bytes[2];  // bytes one pipeline stage receives in both CTAs together
@@ -214,21 +228,34 @@ __device__ __forceinline__ void sched_release(Ctl* ctl, int slot) {
   mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->sempty[slot]), 0));
 }
 
-template <int MODE>
+// Loads this CTA's part of one operand for K block k0 into `dst`.
+__device__ __forceinline__ void load_operand(uint8_t* dst, const CUtensorMap* m, int mode,
+                                             uint32_t fb, int mn0, int mn_count, int k0) {
+  if (mode == kLoadK) {
+    tma_load_2d_pair(dst, m, fb, k0, mn0);
+  } else if (mode == kLoadMN3d) {
+    tma_load_3d_pair(dst, m, fb, 0, k0, mn0 / 64);
+  } else {
+    for (int a = 0; a < (mn_count + 63) / 64; ++a)
+      tma_load_2d_pair(dst + a * kAtomBytes, m, fb, mn0 + a * 64, k0);
+  }
+}
+
+// TMA producer of operand A (OPERAND = 0, warp 0) or B (OPERAND = 1, warp 10).
+// The first CTA's A producer also runs the tile ring: it takes tile numbers
+// from the global counter and pushes them to every role of both CTAs.
+template <int MODE, int OPERAND>
 __device__ void producer_loop(const KParams& P, const Sizes& S, uint8_t* smem, Ctl* ctl,
                               const WaitCtx& wc, uint32_t rank) {
   int stage = 0;
   uint32_t phase = 0;
   int slot = 0;
   uint32_t sphase = 0;
-  uint32_t issued[kStages];
-#pragma unroll
-  for (int s = 0; s < kStages; ++s) issued[s] = 0;
   bool aborted = false;
-  const bool leader = rank == 0;
+  const bool ring_head = (OPERAND == 0) && rank == 0;
   while (true) {
     int t;
-    if (leader) {
+    if (ring_head) {
       if (!mbar_wait(&ctl->sempty[slot], sphase ^ 1u, wc)) {
         aborted = true;
         break;
@@ -250,37 +277,28 @@ __device__ void producer_loop(const KParams& P, const Sizes& S, uint8_t* smem, C
     if (t < 0) break;
     const Tile tl = decode_tile<MODE>(S, t);
     const int pi = tl.prob;
-    const CUtensorMap* ma = &P.tmA[pi];
-    const CUtensorMap* mb = &P.tmB[pi];
-    const int bn_half = S.bn[pi] >> 1;
-    const int a_row0 = tl.m * kPairM + static_cast<int>(rank) * kBM;
-    const int b_col0 = tl.n * S.bn[pi] + static_cast<int>(rank) * bn_half;
+    const CUtensorMap* m = OPERAND == 0 ? &P.tmA[pi] : &P.tmB[pi];
+    const int mode = OPERAND == 0 ? P.a_load[pi] : P.b_load[pi];
+    int mn0, mn_count;
+    if (OPERAND == 0) {
+      mn0 = tl.m * kPairM + static_cast<int>(rank) * kBM;
+      mn_count = kBM;
+    } else {
+      mn_count = S.bn[pi] >> 1;
+      mn0 = tl.n * S.bn[pi] + static_cast<int>(rank) * mn_count;
+    }
+    const uint32_t tx = P.tx_bytes[pi];
     for (int kb = 0; kb < tl.nkb; ++kb) {
-      if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, wc)) {
+      if (!mbar_wait_fast(&ctl->empty[stage], phase ^ 1u, wc)) {
         aborted = true;
         break;
       }
-      uint8_t* sa = smem + stage * kStageBytes;
-      uint8_t* sb = sa + kABytes;
-      // Both CTAs' copies complete on the first CTA's barrier, which expects
-      // the bytes of both.
-      if (leader) mbar_arrive_expect_tx(&ctl->full[stage], P.tx_bytes[pi]);
+      // Both CTAs' copies of A and B complete on the first CTA's barrier,
+      // which expects the bytes of all four.
+      if (OPERAND == 0 && rank == 0) mbar_arrive_expect_tx(&ctl->full[stage], tx);
       const uint32_t fb = mapa_shared(smem_u32(&ctl->full[stage]), 0);
-      const int k0 = kb * kBK;
-      if (P.a_mn[pi]) {
-#pragma unroll
-        for (int a = 0; a < kBM / 64; ++a)
-          tma_load_2d_pair(sa + a * kAtomBytes, ma, fb, a_row0 + a * 64, k0);
-      } else {
-        tma_load_2d_pair(sa, ma, fb, k0, a_row0);
-      }
-      if (P.b_mn[pi]) {
-        for (int a = 0; a < (bn_half + 63) / 64; ++a)
-          tma_load_2d_pair(sb + a * kAtomBytes, mb, fb, b_col0 + a * 64, k0);
-      } else {
-        tma_load_2d_pair(sb, mb, fb, k0, b_col0);
-      }
-      issued[stage] += 1;
+      uint8_t* dst = smem + stage * kStageBytes + (OPERAND == 0 ? 0 : kABytes);
+      load_operand(dst, m, mode, fb, mn0, mn_count, kb * kBK);
       if (++stage == kStages) {
         stage = 0;
         phase ^= 1u;
@@ -289,18 +307,12 @@ __device__ void producer_loop(const KParams& P, const Sizes& S, uint8_t* smem, C
     if (aborted) break;
   }
   if (aborted) {
-    // Let the copies already issued land before the CTA's shared memory goes
-    // away.  Their completion is counted in the first CTA only, so the second
-    // CTA just waits a fixed 20 ms (a copy takes microseconds).
-    if (leader) {
-#pragma unroll
-      for (int s = 0; s < kStages; ++s)
-        if (issued[s] != 0)
-          mbar_wait_drain(&ctl->full[s], (issued[s] - 1u) & 1u, P.err, 20000000ull);
-    } else {
-      const uint64_t t0 = globaltimer_ns();
-      while (globaltimer_ns() - t0 < 20000000ull) {
-      }
+    // Let copies already issued land before the CTA's shared memory goes
+    // away.  Their completion is counted in the first CTA's barriers, which
+    // the other roles may no longer be waiting on, so wait a fixed 20 ms (a
+    // copy takes microseconds).
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 20000000ull) {
     }
   }
 }
@@ -335,7 +347,7 @@ __device__ void mma_loop(const KParams& P, const Sizes& S, uint8_t* smem, Ctl* c
     const uint32_t idesc = idesc_bf16_f32(kPairM, S.bn[pi], a_mn, b_mn);
     bool ok = true;
     for (int kb = 0; kb < tl.nkb; ++kb) {
-      if (!mbar_wait(&ctl->full[stage], phase, wc)) {
+      if (!mbar_wait_fast(&ctl->full[stage], phase, wc)) {
         ok = false;
         break;
       }
@@ -648,9 +660,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   const WaitCtx wc{&ctl->abort, mapa_shared(smem_u32(&ctl->abort), rank ^ 1u), P.err};
 
   if (warp == 0) {
-    if (lane == 0) producer_loop<MODE>(P, S, smem, ctl, wc, rank);
+    if (lane == 0) producer_loop<MODE, 0>(P, S, smem, ctl, wc, rank);
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) mma_loop<MODE>(P, S, smem, ctl, tmem, wc);
+  } else if (warp == kBProducerWarp) {
+    if (lane == 0) producer_loop<MODE, 1>(P, S, smem, ctl, wc, rank);
   } else {
     if (MODE == kModePass1)
       epilogue_pass1(P, S, ctl, tmem, wc, warp, lane, static_cast<int>(rank));
@@ -709,10 +723,27 @@ int tile_width(int64_t N) {
   return static_cast<int>((w + 15) / 16 * 16);
 }
 
-bool encode_operand(CUtensorMap* m, const void* base, int mn, int64_t inner, int64_t outer,
+// Encodes the tensor map of one operand for the given load mode (see
+// load_operand); rows_per_tile is this CTA's share of the tile along M or N.
+bool encode_operand(CUtensorMap* m, const void* base, int mode, int64_t inner, int64_t outer,
                     int64_t ld, int rows_per_tile) {
-  if (mn) return encode_tmap_bf16(m, base, inner, outer, ld, 64, kBK);
-  return encode_tmap_bf16(m, base, inner, outer, ld, kBK, rows_per_tile);
+  if (mode == kLoadK) return encode_tmap_bf16(m, base, inner, outer, ld, kBK, rows_per_tile);
+  if (mode == kLoadMN3d)
+    return encode_tmap_bf16_mn3d(m, base, inner, outer, ld, rows_per_tile / 64, kBK);
+  return encode_tmap_bf16(m, base, inner, outer, ld, 64, kBK);
+}
+
+// Load mode of an operand: MN-major tiles use one 3-D box when the stored
+// rows are whole atoms and every CTA's part starts on an atom (its share of
+// the tile is a multiple of 64).
+int load_mode(int mn, int64_t inner, int share) {
+  if (!mn) return kLoadK;
+  return (inner % 64 == 0 && share % 64 == 0) ? kLoadMN3d : kLoadMN2d;
+}
+
+uint32_t stage_bytes(int mode, int share) {
+  if (mode == kLoadK) return static_cast<uint32_t>(share) * kBK * 2;
+  return static_cast<uint32_t>((share + 63) / 64) * kAtomBytes;
 }
 
 }  // namespace
@@ -723,16 +754,18 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& g, cudaStream_t s) {
   for (int pi = 0; pi < g.nprob; ++pi) {
     const TcProblem& q = g.pr[pi];
     const int bn = tile_width(q.N);
-    if (!encode_operand(&P.tmA[pi], q.A, q.a_mn, q.a_inner, q.a_outer, q.lda, kBM) ||
-        !encode_operand(&P.tmB[pi], q.B, q.b_mn, q.b_inner, q.b_outer, q.ldb, bn / 2))
+    // each CTA: its 128 rows of A and its bn/2 columns of B
+    const int a_load = load_mode(q.a_mn, q.a_inner, kBM);
+    const int b_load = load_mode(q.b_mn, q.b_inner, bn / 2);
+    if (!encode_operand(&P.tmA[pi], q.A, a_load, q.a_inner, q.a_outer, q.lda, kBM) ||
+        !encode_operand(&P.tmB[pi], q.B, b_load, q.b_inner, q.b_outer, q.ldb, bn / 2))
       return cudaErrorInvalidValue;
     P.a_mn[pi] = q.a_mn;
     P.b_mn[pi] = q.b_mn;
+    P.a_load[pi] = a_load;
+    P.b_load[pi] = b_load;
     P.bn[pi] = bn;
-    // each CTA: its 128 rows of A and its bn/2 columns of B
-    const uint32_t b_bytes = q.b_mn ? static_cast<uint32_t>((bn / 2 + 63) / 64) * kAtomBytes
-                                    : static_cast<uint32_t>(bn / 2) * kBK * 2;
-    P.tx_bytes[pi] = 2u * (kABytes + b_bytes);
+    P.tx_bytes[pi] = 2u * (stage_bytes(a_load, kBM) + stage_bytes(b_load, bn / 2));
     P.M[pi] = static_cast<int>(q.M);
     P.N[pi] = static_cast<int>(q.N);
     P.K[pi] = static_cast<int>(q.K);
@@ -759,9 +792,10 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& g, cudaStream_t s) {
 cudaError_t launch_tc_pass1(const Pass1Args& p, const ChunkArgs& a, cudaStream_t s) {
   KParams P;
   memset(&P, 0, sizeof(P));
-  if (!encode_operand(&P.tmA[0], p.hc, 0, p.d, a.cpad, p.d, kBM) ||
-      !encode_operand(&P.tmB[0], p.W, 0, p.d, a.V, p.d, kBN / 2))
+  if (!encode_operand(&P.tmA[0], p.hc, kLoadK, p.d, a.cpad, p.d, kBM) ||
+      !encode_operand(&P.tmB[0], p.W, kLoadK, p.d, a.V, p.d, kBN / 2))
     return cudaErrorInvalidValue;
+  P.a_load[0] = P.b_load[0] = kLoadK;
   P.tmA[1] = P.tmA[0];
   P.tmB[1] = P.tmB[0];
   P.M[0] = a.chunk;
