@@ -135,7 +135,7 @@ struct KParams {
 };
 
 struct Sizes {
-  int M[2], N[2], nkb[2], mt[2], nt[2], tiles[2], bn[2];
+  int M[2], N[2], nkb[2], mt[2], nt[2], tiles[2], bn[2], b3d[2];
   int total;
   int count;
 };
@@ -159,6 +159,7 @@ __device__ __forceinline__ Sizes get_sizes(const KParams& P) {
     s.nkb[pi] = (K + kBK - 1) / kBK;
     s.mt[pi] = (M + kPairM - 1) / kPairM;
     s.bn[pi] = P.bn[pi];
+    s.b3d[pi] = P.b_load[pi] == kLoadMN3d;
     s.nt[pi] = s.bn[pi] > 0 ? (N + s.bn[pi] - 1) / s.bn[pi] : 0;
     int tiles = s.mt[pi] * s.nt[pi];
     if (pi >= P.nprob) tiles = 0;
@@ -172,6 +173,7 @@ __device__ __forceinline__ Sizes get_sizes(const KParams& P) {
 
 struct Tile {
   int prob, m, n, nkb;
+  int n_cols;  // MMA width of this tile: bn, or less for the last column tile
 };
 
 // Pass 1 walks the vocabulary slowly (m fastest) so that the CTAs running at
@@ -194,6 +196,12 @@ __device__ __forceinline__ Tile decode_tile(const Sizes& S, int t) {
     tl.m = t / S.nt[pi];
   }
   tl.nkb = S.nkb[pi];
+  // The pair MMA takes B as two halves of n_cols / 2 columns, one from each
+  // CTA; a 3-D loaded B half must start on a 64-column atom (n_cols a
+  // multiple of 128), any other B half on 8 columns (n_cols a multiple of 16).
+  const int n_rest = S.N[pi] - tl.n * S.bn[pi];
+  const int gran = S.b3d[pi] ? 128 : 16;
+  tl.n_cols = min(S.bn[pi], (n_rest + gran - 1) / gran * gran);
   return tl;
 }
 
@@ -284,8 +292,9 @@ __device__ void producer_loop(const KParams& P, const Sizes& S, uint8_t* smem, C
       mn0 = tl.m * kPairM + static_cast<int>(rank) * kBM;
       mn_count = kBM;
     } else {
+      // boxes cover the problem's half tile; this tile's halves may be narrower
       mn_count = S.bn[pi] >> 1;
-      mn0 = tl.n * S.bn[pi] + static_cast<int>(rank) * mn_count;
+      mn0 = tl.n * S.bn[pi] + static_cast<int>(rank) * (tl.n_cols >> 1);
     }
     const uint32_t tx = P.tx_bytes[pi];
     for (int kb = 0; kb < tl.nkb; ++kb) {
@@ -344,7 +353,7 @@ __device__ void mma_loop(const KParams& P, const Sizes& S, uint8_t* smem, Ctl* c
     const uint32_t d_tmem = tmem + static_cast<uint32_t>(b * kBN);
     const int pi = tl.prob;
     const int a_mn = P.a_mn[pi], b_mn = P.b_mn[pi];
-    const uint32_t idesc = idesc_bf16_f32(kPairM, S.bn[pi], a_mn, b_mn);
+    const uint32_t idesc = idesc_bf16_f32(kPairM, tl.n_cols, a_mn, b_mn);
     bool ok = true;
     for (int kb = 0; kb < tl.nkb; ++kb) {
       if (!mbar_wait_fast(&ctl->full[stage], phase, wc)) {
@@ -714,10 +723,14 @@ cudaError_t launch_mode(const KParams& P, int num_sms, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<MODE>, P);
 }
 
-// Output tile width for an N-wide output: the fewest 256-wide tiles, then
-// the narrowest multiple of 16 that still covers N with that many tiles
-// (d = 2880 -> 12 tiles of 240 instead of 11.25 tiles of 256).
-int tile_width(int64_t N) {
+// Output tile width for an N-wide output.  An MN-major B whose rows are whole
+// 64-element atoms takes 256-wide tiles, so each CTA's half starts on an atom
+// and loads with one 3-D box (the last tile multiplies only its real
+// columns).  Otherwise: the fewest 256-wide tiles, then the narrowest multiple
+// of 16 that still covers N with that many tiles (d = 2880 -> 12 tiles of 240
+// instead of 11.25 tiles of 256).
+int tile_width(int64_t N, int b_mn, int64_t b_inner) {
+  if (b_mn && b_inner % 64 == 0) return kBN;
   const int64_t tiles = (N + kBN - 1) / kBN;
   const int64_t w = (N + tiles - 1) / tiles;
   return static_cast<int>((w + 15) / 16 * 16);
@@ -753,7 +766,7 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& g, cudaStream_t s) {
   memset(&P, 0, sizeof(P));
   for (int pi = 0; pi < g.nprob; ++pi) {
     const TcProblem& q = g.pr[pi];
-    const int bn = tile_width(q.N);
+    const int bn = tile_width(q.N, q.b_mn, q.b_inner);
     // each CTA: its 128 rows of A and its bn/2 columns of B
     const int a_load = load_mode(q.a_mn, q.a_inner, kBM);
     const int b_load = load_mode(q.b_mn, q.b_inner, bn / 2);
