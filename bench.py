@@ -46,6 +46,65 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+# Kernel sources whose DRAM traffic a committed ncu capture describes; the
+# capture applies only while these files are unchanged.
+TRAFFIC_SOURCES = ["top_kl_loss_token_b300/csrc/kd_tc_gemm.cu",
+                   "top_kl_loss_token_b300/csrc/kd_ptx.cuh",
+                   "top_kl_loss_token_b300/csrc/kd_internal.h",
+                   "top_kl_loss_token_b300/csrc/kd_api.cu"]
+TRAFFIC_PROFILE = "profiles/dram_traffic_vocab201k-32k.md"
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(kernel: str, workload: str, chunk: int):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or
+    None when it was taken on other sources or another workload."""
+    import re
+    path = os.path.join(ROOT, TRAFFIC_PROFILE)
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"^source-sha256: ([0-9a-f]{64})$", text, re.M)
+    w = re.search(r"^workload: (.+)$", text, re.M)
+    b = re.search(r"^%s: ([0-9]+) bytes per launch" % re.escape(kernel), text, re.M)
+    if not (m and w and b) or m.group(1) != kernel_source_hash():
+        return None
+    if w.group(1).strip() != f"{workload}; chunk {chunk}":
+        return None
+    return int(b.group(1))
+
+
+def hbm_kernel_bytes(x, chunk: int, valid: int) -> dict:
+    """Algorithmic DRAM bytes per launch of the bandwidth-bound kernels (each
+    input read once, each output written once)."""
+    N, d, V, K = x.N, x.d, x.V, x.K
+    n_pb = -(-V // 128)
+    ldg = -(-V // 256) * 256
+    c = min(chunk, valid) if valid else 0
+    n_chunks = max(1, -(-valid // chunk)) if valid else 1
+    c_avg = valid / n_chunks if valid else 0
+    return {
+        # topk_idx and topk_logit read, sorted (index, p) lists written
+        "teacher_prep": 16.0 * N * K,
+        # u read and G written (bf16), per-(row, block) alpha and offsets, sorted lists
+        "grad_tile": c_avg * (4.0 * ldg + 6.0 * n_pb + 8.0 * K),
+        # three per-(row, block) statistics read, alpha written
+        "lse_combine": c_avg * 16.0 * n_pb,
+        # sorted indices read, per-(row, block) offsets written
+        "bucket_offsets": c_avg * (4.0 * K + 2.0 * (n_pb + 1)),
+        # the chunk's h rows read and written contiguously
+        "gather_rows": c_avg * 4.0 * d,
+    }
+
+
 def workload_name(x) -> str:
     mask = f", {x.masked_fraction() * 100:.1f}% masked" if x.mask is not None else ""
     return (f"{x.name}: N={x.N} tokens, d={x.d}, V={x.V}, K={x.K}, T={x.T:g}, "
@@ -146,6 +205,59 @@ def run_reference(args, x):
     print(json.dumps(line), flush=True)
 
 
+def shard_seed(seed: int, rank: int, world: int) -> int:
+    """Seed of this rank's token shard: every rank draws its own tokens of the
+    same sizes (weak scaling); a single process keeps the workload's seed."""
+    return seed if world <= 1 else seed + 1000 * rank
+
+
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time (the whole job ends when the last rank does)."""
+    if world <= 1:
+        return float(ms)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_mem_scaling(args):
+    """Device memory of one fused fwd+bwd at the 201,088-vocabulary shapes for
+    N = 8K, 32K and 128K tokens at a fixed 8192-token chunk.  Extra memory (the
+    workspace) must grow as O(chunk V + N K), not O(N V).  Values of the inputs
+    do not matter here, so they are drawn on the device."""
+    import torch
+    import top_kl_loss_token_b300 as kd
+    kd.load_library()
+    dev = torch.device("cuda", 0)
+    d, V, K, chunk = 2880, 201088, 100, args.chunk or 8192
+    g = torch.Generator(device=dev).manual_seed(0)
+    W = (torch.randn(V, d, device=dev, generator=g) * 0.02).to(torch.bfloat16)
+    out = []
+    for N in (8192, 32768, 131072):
+        h = torch.randn(N, d, device=dev, generator=g).to(torch.bfloat16)
+        idx = torch.randint(0, V, (N, K), device=dev, generator=g, dtype=torch.int32)
+        lg = torch.randn(N, K, device=dev, generator=g)
+        loss = torch.empty(1, device=dev)
+        gh = torch.empty(N, d, device=dev)
+        gW = torch.empty(V, d, device=dev)
+        torch.cuda.synchronize(dev)
+        base = torch.cuda.memory_allocated(dev)
+        torch.cuda.reset_peak_memory_stats(dev)
+        ws = kd.allocate_workspace(N, d, V, K, chunk, kd.KD_BF16, dev)
+        kd.fwd_bwd(h, W, idx, lg, None, 1.0, chunk, loss=loss, grad_h=gh, grad_W=gW, workspace=ws)
+        torch.cuda.synchronize(dev)
+        peak = torch.cuda.max_memory_allocated(dev)
+        out.append({"N": N, "chunk": chunk, "workspace_gib": ws.numel() / 2 ** 30,
+                    "peak_extra_gib": (peak - base) / 2 ** 30,
+                    "inputs_outputs_gib": base / 2 ** 30,
+                    "dense_bf16_logits_gib": N * V * 2 / 2 ** 30})
+        del h, idx, lg, loss, gh, gW, ws
+        torch.cuda.empty_cache()
+    print(json.dumps({"mem_scaling": out, "d": d, "V": V, "K": K}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -161,6 +273,8 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=64,
                     help="tokens per step of the reference (oracle) arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mem-scaling", action="store_true",
+                    help="report device memory at N = 8K, 32K, 128K tokens (fixed chunk) and exit")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -181,6 +295,10 @@ def main():
     import torch.distributed as dist
     import top_kl_loss_token_b300 as kd
 
+    if args.mem_scaling:
+        run_mem_scaling(args)
+        return
+
     if world > 1:
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
@@ -193,9 +311,7 @@ def main():
         c["N"] = args.tokens
         if c.get("mask") == "packed":
             c["mask_frac_range"] = None
-    if world > 1:
-        # each rank's token shard: same sizes, its own seed
-        c["seed"] = c["seed"] + 1000 * rank
+    c["seed"] = shard_seed(c["seed"], rank, world)
     x = synth.make_inputs(**c)
     N, d, V, K = x.N, x.d, x.V, x.K
     dt_code = kd.KD_BF16 if x.dtype == "bf16" else kd.KD_FP32
@@ -256,11 +372,7 @@ def main():
         barrier()
     kd.timing_enable(False)
     kernels = kd.timing_collect()
-    ms = ev0.elapsed_time(ev1)
-    ms_t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms = float(ms_t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
     tokens_total = N * args.steps * world
     value = tokens_total / (ms / 1000.0)
     flops_step = 6.0 * N * d * V
@@ -289,10 +401,7 @@ def main():
     e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
-    e_ms = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(e_ms, op=dist.ReduceOp.MAX)
-    e_value = N * e_steps * world / (float(e_ms.item()) / 1000.0)
+    e_value = N * e_steps * world / (max_over_ranks(e0.elapsed_time(e1), world, dev) / 1000.0)
 
     if rank != 0:
         if world > 1:
@@ -312,12 +421,23 @@ def main():
         flops_per_launch = per_token[dom] * valid_tokens * args.steps / launches
         achieved = flops_per_launch / (tot_ms / launches / 1000.0) / 1e12
         peak = peaks["bf16_tflops_sustained"]
+        traffic = None
+        if not args.tokens and args.config == 3:
+            traffic = measured_traffic(dom, x.name, chunk)
         roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                 "peak_source": f"{peaks_src} bf16 sustained (kernel timed inside a long step)",
                 "flops_per_launch": flops_per_launch,
                 "avg_launch_ms": tot_ms / launches}
     launches_total = sum(v[0] for v in kernels.values())
+    hbm = {}
+    for name, nbytes in hbm_kernel_bytes(x, chunk, valid_tokens).items():
+        if name not in kernels:
+            continue
+        launches, tot_ms = kernels[name]
+        gbs = nbytes / (tot_ms / launches / 1000.0) / 1e9
+        hbm[name] = {"bytes_per_launch": nbytes, "ms_per_launch": tot_ms / launches,
+                     "achieved_gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"]}
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -338,6 +458,8 @@ def main():
         "pct_of_bf16_peak": {"burst": tflops / peaks["bf16_tflops"],
                              "sustained": tflops / peaks["bf16_tflops_sustained"],
                              "source": peaks_src},
+        "tflops_valid_tokens_per_gpu": 6.0 * valid_tokens * d * V * args.steps / (ms / 1000.0) / 1e12,
+        "hbm_kernels": hbm,
         "peak_extra_gib": peak_extra,
         "workspace_gib": ws_bytes / 2 ** 30,
         "roofline": roof,

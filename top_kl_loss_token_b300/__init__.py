@@ -269,6 +269,34 @@ def kd_timing_collect():
             for i in range(min(n.value, 32))}
 
 
+def dp_combine(loss, grad_h, grad_W, n_valid: int, group=None):
+    """Token-sharded data parallelism: each rank ran kd_topk_kl_fwd_bwd on its
+    own tokens, so its loss is the mean over its N_valid,r valid tokens and its
+    gradients carry 1/(T N_valid,r).  The loss of the whole batch is the mean
+    over all valid tokens, so every rank's results are reweighted by
+    N_valid,r / sum_r N_valid,r; then loss and grad_W are summed across ranks
+    (grad_h rows stay with their rank).  This is the one exchange the sharded
+    loss needs; grad_W's sum is the data-parallel gradient reduction a training
+    loop performs anyway.
+
+    loss [1] fp32, grad_h [N_r, d] fp32, grad_W [V, d] fp32 (updated in place);
+    n_valid: this rank's valid-token count.  Returns (loss, grad_h, grad_W)."""
+    import torch
+    import torch.distributed as dist
+    dev = grad_W.device
+    nv = torch.tensor([float(n_valid)], dtype=torch.float64, device=dev)
+    dist.all_reduce(nv, group=group)
+    total = float(nv.item())
+    w = float(n_valid) / total if total > 0 else 0.0
+    lw = (loss.to(torch.float64) * w).to(dev)
+    dist.all_reduce(lw, group=group)
+    loss.copy_(lw.to(loss.dtype))
+    grad_h.mul_(w)
+    grad_W.mul_(w)
+    dist.all_reduce(grad_W, group=group)
+    return loss, grad_h, grad_W
+
+
 def status_string(st: int) -> str:
     return load_library().kd_status_string(st).decode()
 
