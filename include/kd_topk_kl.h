@@ -82,6 +82,9 @@ typedef enum { KD_BF16 = 0, KD_FP32 = 1 } kd_dtype;
 #define KD_FLAG_INDEX_RANGE 1u
 #define KD_FLAG_BAD_TEACHER 2u
 #define KD_FLAG_TIMEOUT 4u
+/* A bound the kernels rely on was found violated (a defect, not a data
+ * error); the results of the call are not valid. */
+#define KD_FLAG_INTERNAL 8u
 
 /* Largest K accepted (the per-row sort of the teacher entries runs in shared
  * memory); larger K returns KD_ERR_UNSUPPORTED. */

@@ -101,3 +101,30 @@ def test_umma_gemm_argument_errors(lib):
 
 def test_build_flags_target_sm103a():
     assert "arch=compute_103a,code=sm_103a" in kd_build.ARCH
+
+
+def test_topk_cache_argument_errors_and_plan(lib):
+    f = lib.kd_topk_cache_build
+    ok = dict(h=256, W=256, N=8, d=16, V=300, K=4, chunk=0, idx=256, val=256, ws=256,
+              ws_bytes=1 << 40)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return f(a["h"], a["W"], a["N"], a["d"], a["V"], a["K"], a["chunk"], a["idx"], a["val"],
+                 a["ws"], a["ws_bytes"], None, None)
+    assert call(W=None) == 1
+    assert call(h=None) == 1
+    assert call(K=0) == 1
+    assert call(K=301) == 1              # K > V
+    assert call(N=-1) == 1
+    assert call(d=12) == 2               # rows must be 16-byte multiples
+    assert call(K=kd.KD_MAX_K + 1, V=10 ** 6) == 2
+    assert call(ws=None) == 3
+    assert call(ws_bytes=10) == 3
+    assert call(h=264) == 1              # misaligned
+    # candidates are bounded by 128 K per row, block keys by V / 128 per row
+    n = kd.topk_cache_workspace_bytes(8192, 2880, 201088, 100, 8192)
+    per_row = 8 * (128 * 100 + 1571 + 1) + 4
+    assert 8192 * per_row <= n <= 8192 * per_row + 4096
+    assert lib.kd_topk_cache_default_chunk(32768, 201088, 100) % 128 == 0

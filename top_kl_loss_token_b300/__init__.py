@@ -26,6 +26,7 @@ KD_FP32 = 1
 KD_FLAG_INDEX_RANGE = 1
 KD_FLAG_BAD_TEACHER = 2
 KD_FLAG_TIMEOUT = 4
+KD_FLAG_INTERNAL = 8
 KD_MAX_K = 4096
 
 STATUS = {0: "KD_OK", 1: "KD_ERR_INVALID_ARG", 2: "KD_ERR_UNSUPPORTED", 3: "KD_ERR_WORKSPACE",
@@ -35,7 +36,8 @@ STATUS = {0: "KD_OK", 1: "KD_ERR_INVALID_ARG", 2: "KD_ERR_UNSUPPORTED", 3: "KD_E
 EXPORTS = ["kd_topk_kl_workspace_bytes", "kd_topk_kl_default_chunk", "kd_topk_kl_fwd_bwd",
            "kd_topk_kl_fwd", "kd_status_string", "kd_topk_kl_workspace_layout",
            "kd_umma_gemm_bf16", "kd_timing_enable", "kd_timing_collect",
-           "kd_topk_kl_fwd_bwd_noalloc"]
+           "kd_topk_kl_fwd_bwd_noalloc", "kd_topk_cache_workspace_bytes",
+           "kd_topk_cache_default_chunk", "kd_topk_cache_build"]
 
 # Size of the library-held scratch array used by kd_topk_kl_fwd_bwd_noalloc.
 KD_NOALLOC_SCRATCH_BYTES = 64 << 20
@@ -88,6 +90,12 @@ def load_library(path: str = LIB_PATH):
     lib.kd_topk_kl_fwd_bwd_noalloc.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, i64, i64, i64,
                                                i32, f32, i64, vp, vp, vp, vp, vp]
     lib.kd_topk_kl_fwd_bwd_noalloc.restype = ctypes.c_int
+    lib.kd_topk_cache_workspace_bytes.argtypes = [i64, i64, i64, i32, i64]
+    lib.kd_topk_cache_workspace_bytes.restype = sz
+    lib.kd_topk_cache_default_chunk.argtypes = [i64, i64, i32]
+    lib.kd_topk_cache_default_chunk.restype = i64
+    lib.kd_topk_cache_build.argtypes = [vp, vp, i64, i64, i64, i32, i64, vp, vp, vp, sz, vp, vp]
+    lib.kd_topk_cache_build.restype = ctypes.c_int
     lib.kd_status_string.argtypes = [ctypes.c_int]
     lib.kd_status_string.restype = ctypes.c_char_p
     lib.kd_umma_gemm_bf16.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.c_int, ctypes.c_int,
@@ -237,6 +245,41 @@ def kd_topk_kl_fwd_bwd_noalloc(h, W, topk_idx, topk_logit, loss, grad_h, grad_W,
     return loss, grad_h, grad_W
 
 
+def topk_cache_workspace_bytes(N: int, d: int, V: int, K: int, chunk: int = 0) -> int:
+    n = load_library().kd_topk_cache_workspace_bytes(N, d, V, K, chunk)
+    if n == 0:
+        raise KDError(1, "kd_topk_cache_workspace_bytes")
+    return int(n)
+
+
+def kd_topk_cache_build(h, W, K: int, chunk: int = 0, topk_idx=None, topk_logit=None,
+                        workspace=None, err_flags=None, stream=None):
+    """The offline teacher top-K cache of teacher hidden states h [N, d] (bf16)
+    against the teacher LM head W [V, d] (bf16); see include/kd_topk_cache.h.
+    Returns (topk_idx [N, K] int32, topk_logit [N, K] fp32, workspace)."""
+    import torch
+    for name, t in (("h", h), ("W", W)):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be a contiguous bfloat16 CUDA tensor")
+    N, d = h.shape
+    V, d2 = W.shape
+    if d2 != d:
+        raise ValueError("shape mismatch")
+    dev = h.device
+    if topk_idx is None:
+        topk_idx = torch.empty((N, K), dtype=torch.int32, device=dev)
+    if topk_logit is None:
+        topk_logit = torch.empty((N, K), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(topk_cache_workspace_bytes(N, d, V, K, chunk), dtype=torch.uint8,
+                                device=dev)
+    st = load_library().kd_topk_cache_build(
+        _ptr(h), _ptr(W), N, d, V, int(K), int(chunk), _ptr(topk_idx), _ptr(topk_logit),
+        _ptr(workspace), workspace.numel(), _ptr(err_flags), _stream_handle(stream))
+    _check(st, "kd_topk_cache_build")
+    return topk_idx, topk_logit, workspace
+
+
 def kd_umma_gemm_bf16(A, B, M: int, N: int, K: int, a_mn_major: bool, b_mn_major: bool,
                       out=None, accumulate: bool = False, err_flags=None, stream=None):
     """D[M, N] (+)= A(m, k) B(n, k) on the tensor cores (see kd_topk_kl_steps.h)."""
@@ -314,5 +357,6 @@ def workspace_view(workspace, lay: WorkspaceLayout, name: str, count: int, dtype
 fwd_bwd = kd_topk_kl_fwd_bwd
 fwd = kd_topk_kl_fwd
 fwd_bwd_noalloc = kd_topk_kl_fwd_bwd_noalloc
+topk_cache_build = kd_topk_cache_build
 timing_enable = kd_timing_enable
 timing_collect = kd_timing_collect

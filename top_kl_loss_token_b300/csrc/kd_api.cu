@@ -50,25 +50,11 @@ int num_sms() {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // ------------------------------------------------------------- kernel timing
-enum Kind {
-  kTeacherPrep,
-  kCompact,
-  kZeroRows,
-  kGatherRows,
-  kBucketOffsets,
-  kPass1Gemm,
-  kLseCombine,
-  kGradTile,
-  kBwdGemm,
-  kFinalize,
-  kSimtPass1,
-  kSimtGemm,
-  kNumKinds
-};
 const char* const kKindNames[kNumKinds] = {
     "teacher_prep", "compact",    "zero_invalid_rows", "gather_rows", "bucket_offsets",
     "pass1_gemm",   "lse_combine", "grad_tile",        "bwd_gemm",    "finalize",
-    "simt_pass1",   "simt_gemm"};
+    "simt_pass1",   "simt_gemm",   "topk_block_max",   "topk_threshold",
+    "topk_candidates", "topk_select"};
 
 struct TimingRec {
   int kind;
@@ -89,27 +75,22 @@ cudaEvent_t pooled_event() {
   return e;
 }
 
-// Brackets one launch with events when timing is on.
-struct TimedLaunch {
-  int kind;
-  cudaStream_t s;
-  cudaEvent_t a = nullptr;
-  TimedLaunch(int k, cudaStream_t st) : kind(k), s(st) {
-    if (g_timing_on) {
-      a = pooled_event();
-      if (a != nullptr) cudaEventRecord(a, s);
-    }
-  }
-  ~TimedLaunch() {
-    if (a == nullptr) return;
-    cudaEvent_t b = pooled_event();
-    if (b == nullptr) return;
-    cudaEventRecord(b, s);
-    g_recs.push_back(TimingRec{kind, a, b});
-  }
-};
-
 }  // namespace
+
+TimedLaunch::TimedLaunch(int k, cudaStream_t st) : kind(k), s(st) {
+  if (g_timing_on) {
+    a = pooled_event();
+    if (a != nullptr) cudaEventRecord(a, s);
+  }
+}
+
+TimedLaunch::~TimedLaunch() {
+  if (a == nullptr) return;
+  cudaEvent_t b = pooled_event();
+  if (b == nullptr) return;
+  cudaEventRecord(b, s);
+  g_recs.push_back(TimingRec{kind, a, b});
+}
 
 bool encode_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                       uint64_t ld_elems, uint32_t box_inner, uint32_t box_outer) {

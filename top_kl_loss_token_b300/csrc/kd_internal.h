@@ -26,6 +26,37 @@ constexpr int kNoIndex = 0x7fffffff;
 __host__ __device__ constexpr int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 __host__ __device__ constexpr int64_t ceil_div(int64_t x, int64_t m) { return (x + m - 1) / m; }
 
+// Kernel kinds, for the optional per-launch timing (kd_timing_enable).
+enum KernelKind {
+  kTeacherPrep,
+  kCompact,
+  kZeroRows,
+  kGatherRows,
+  kBucketOffsets,
+  kPass1Gemm,
+  kLseCombine,
+  kGradTile,
+  kBwdGemm,
+  kFinalize,
+  kSimtPass1,
+  kSimtGemm,
+  kTopkBlockMax,
+  kTopkThreshold,
+  kTopkCandidates,
+  kTopkSelect,
+  kNumKinds
+};
+
+// Brackets one kernel launch with CUDA events on its stream while timing is
+// enabled (host-side state shared by all calls; not thread-safe).
+struct TimedLaunch {
+  TimedLaunch(int kind, cudaStream_t s);
+  ~TimedLaunch();
+  int kind;
+  cudaStream_t s;
+  cudaEvent_t a = nullptr;
+};
+
 // Workspace plan for one call; all offsets 256-byte aligned.
 struct Plan {
   int64_t N, d, V, K, chunk, cpad, n_pb, ldg, n_chunks;
@@ -163,5 +194,24 @@ struct TcGemmArgs {
   int num_sms;
 };
 cudaError_t launch_tc_gemm(const TcGemmArgs& g, cudaStream_t s);
+
+// Teacher top-K cache: the two tensor-core passes over one chunk of positions
+// (z = h_c W^T).  pass 1 stores each 128-column block's largest rank key;
+// pass 2 recomputes the same tiles and appends the keys that reach the row's
+// threshold.
+struct TopkGemmArgs {
+  const void* h;      // [count, d] bf16, the chunk's first row
+  const void* W;      // [V, d] bf16
+  int64_t count, d, V;
+  uint64_t* bkey;     // [count][ceil(V / 128)]
+  const uint64_t* tau;
+  uint32_t* cnt;
+  uint64_t* cand;     // [count][cap]
+  int64_t cap;
+  uint32_t* counter;
+  uint32_t* err;
+  int num_sms;
+};
+cudaError_t launch_tc_topk(const TopkGemmArgs& g, int pass, cudaStream_t s);
 
 }  // namespace kd

@@ -94,7 +94,7 @@ enum : int {
   kLoadMN3d = 2   // MN-major, atom-aligned: one 3-D box covering every atom
 };
 
-enum : int { kModePass1 = 0, kModeStore = 1 };
+enum : int { kModePass1 = 0, kModeStore = 1, kModeTopkMax = 2, kModeTopkCand = 3 };
 
 struct KParams {
   CUtensorMap tmA[2];
@@ -132,6 +132,12 @@ struct KParams {
   float* part_ps;
   uint16_t* u;
   int64_t ldg;
+  // top-K cache epilogues (rows are the chunk's positions, columns the vocabulary)
+  uint64_t* bkey;        // [count][n_pb] largest rank key of each 128-column block
+  const uint64_t* tau;   // [count] rank key of the K-th largest block key
+  uint32_t* cnt;         // [count] candidates appended so far
+  uint64_t* cand;        // [count][cap] candidate rank keys
+  int64_t cap;
 };
 
 struct Sizes {
@@ -188,7 +194,7 @@ __device__ __forceinline__ Tile decode_tile(const Sizes& S, int t) {
     t -= S.tiles[0];
   }
   const int pi = tl.prob;
-  if (MODE == kModePass1) {
+  if (MODE == kModePass1 || MODE == kModeTopkMax || MODE == kModeTopkCand) {
     tl.m = t % S.mt[pi];
     tl.n = t / S.mt[pi];
   } else {
@@ -618,6 +624,116 @@ __device__ void epilogue_pass1(const KParams& P, const Sizes& S, Ctl* ctl, uint3
   }
 }
 
+// Rank key of logit z at vocabulary index v: a larger key ranks first.  The
+// high word orders the float (NaN lowest, -0 folded into +0), the low word
+// puts the lower index first among equal logits.
+__device__ __forceinline__ uint64_t rank_key(float z, uint32_t v) {
+  uint32_t u = __float_as_uint(z);
+  if (z == 0.0f) u = 0u;
+  uint32_t o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  if (z != z) o = 0u;
+  return (static_cast<uint64_t>(o) << 32) | static_cast<uint64_t>(0xFFFFFFFFu - v);
+}
+
+template <int N>
+__device__ __forceinline__ uint64_t max_key32(const float (&v)[N], int col, int nvalid,
+                                              uint64_t best) {
+#pragma unroll
+  for (int j = 0; j < N; ++j) {
+    if (j < nvalid) {
+      const uint64_t k = rank_key(v[j], static_cast<uint32_t>(col + j));
+      best = k > best ? k : best;
+    }
+  }
+  return best;
+}
+
+__device__ __forceinline__ void append_ge(const float (&v)[32], int col, int nvalid, uint64_t tau,
+                                          uint32_t* cnt, uint64_t* cand, int64_t cap,
+                                          uint32_t* err) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    if (j < nvalid) {
+      const uint64_t k = rank_key(v[j], static_cast<uint32_t>(col + j));
+      if (k >= tau) {
+        const uint32_t slot = atomicAdd(cnt, 1u);
+        if (slot < cap) cand[slot] = k;
+        else atomicOr(err, KD_FLAG_INTERNAL);
+      }
+    }
+  }
+}
+
+// Top-K cache epilogues.  Each thread owns one row and one 128-column block
+// of the tile.
+//   kModeTopkMax:  the block's largest rank key -> bkey[row][block];
+//   kModeTopkCand: if the block's largest key reaches the row's threshold
+//                  tau, append every key >= tau to the row's candidates.
+template <int MODE>
+__device__ void epilogue_topk(const KParams& P, const Sizes& S, Ctl* ctl, uint32_t tmem,
+                              const WaitCtx& wc, int warp, int lane, int rank) {
+  const int q = warp & 3;
+  const int half = (warp - 2) >> 2;
+  int slot = 0;
+  uint32_t sphase = 0;
+  int it = 0;
+  while (true) {
+    int t = -1;
+    bool ok = sched_pop(ctl, slot, sphase, t, wc);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) break;
+    __syncwarp();
+    if (lane == 0) sched_release(ctl, slot);
+    if (++slot == kSched) {
+      slot = 0;
+      sphase ^= 1u;
+    }
+    if (t < 0) break;
+    const Tile tl = decode_tile<MODE>(S, t);
+    const int b = it & 1;
+    const uint32_t tp = (static_cast<uint32_t>(it) >> 1) & 1u;
+    ++it;
+    const int i = tl.m * kPairM + rank * kBM + q * 32 + lane;  // row of the chunk
+    const int col0 = tl.n * kBN + half * 128;
+    const int pb = tl.n * 2 + half;
+    const bool live = (i < S.count) && (pb < P.n_pb);
+    bool scan = live;
+    uint64_t tau = 0;
+    if (MODE == kModeTopkCand && live) {
+      tau = P.tau[i];
+      scan = P.bkey[static_cast<int64_t>(i) * P.n_pb + pb] >= tau;
+    }
+    ok = mbar_wait(&ctl->tfull[b], tp, wc);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) break;
+    tc_fence_after();
+    const uint32_t ta = tmem + (static_cast<uint32_t>(q * 32) << 16) +
+                        static_cast<uint32_t>(b * kBN + half * 128);
+    float v0[32], v1[32], v2[32], v3[32];
+    load_acc128(ta, v0, v1, v2, v3);
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->tempty[b]), 0));
+    if (!scan) continue;
+    const int nv = min(128, P.V - col0);
+    if (MODE == kModeTopkMax) {
+      uint64_t best = 0;
+      best = max_key32(v0, col0, nv, best);
+      best = max_key32(v1, col0 + 32, nv - 32, best);
+      best = max_key32(v2, col0 + 64, nv - 64, best);
+      best = max_key32(v3, col0 + 96, nv - 96, best);
+      P.bkey[static_cast<int64_t>(i) * P.n_pb + pb] = best;
+    } else {
+      uint32_t* cnt = P.cnt + i;
+      uint64_t* cand = P.cand + static_cast<int64_t>(i) * P.cap;
+      append_ge(v0, col0, nv, tau, cnt, cand, P.cap, P.err);
+      append_ge(v1, col0 + 32, nv - 32, tau, cnt, cand, P.cap, P.err);
+      append_ge(v2, col0 + 64, nv - 64, tau, cnt, cand, P.cap, P.err);
+      append_ge(v3, col0 + 96, nv - 96, tau, cnt, cand, P.cap, P.err);
+    }
+  }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ KParams P) {
   extern __shared__ uint8_t smem_raw[];
@@ -677,8 +793,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   } else {
     if (MODE == kModePass1)
       epilogue_pass1(P, S, ctl, tmem, wc, warp, lane, static_cast<int>(rank));
-    else
+    else if (MODE == kModeStore)
       epilogue_store(P, S, ctl, tmem, wc, warp, lane, static_cast<int>(rank));
+    else
+      epilogue_topk<MODE>(P, S, ctl, tmem, wc, warp, lane, static_cast<int>(rank));
   }
 
   // No CTA leaves while the other may still arrive on its barriers or have
@@ -840,6 +958,37 @@ cudaError_t launch_tc_pass1(const Pass1Args& p, const ChunkArgs& a, cudaStream_t
   cudaError_t e = cudaMemsetAsync(p.counter, 0, sizeof(uint32_t), s);
   if (e != cudaSuccess) return e;
   return launch_mode<kModePass1>(P, p.num_sms, s);
+}
+
+cudaError_t launch_tc_topk(const TopkGemmArgs& g, int pass, cudaStream_t s) {
+  KParams P;
+  memset(&P, 0, sizeof(P));
+  if (!encode_operand(&P.tmA[0], g.h, kLoadK, g.d, g.count, g.d, kBM) ||
+      !encode_operand(&P.tmB[0], g.W, kLoadK, g.d, g.V, g.d, kBN / 2))
+    return cudaErrorInvalidValue;
+  P.tmA[1] = P.tmA[0];
+  P.tmB[1] = P.tmB[0];
+  P.a_load[0] = P.b_load[0] = kLoadK;
+  P.M[0] = static_cast<int>(g.count);
+  P.N[0] = static_cast<int>(g.V);
+  P.K[0] = static_cast<int>(g.d);
+  P.bn[0] = kBN;  // the epilogue's 128-column blocks need full 256-wide tiles
+  P.tx_bytes[0] = 2u * kStageBytes;
+  P.nprob = 1;
+  P.chunk = static_cast<int>(g.count);
+  P.counter = g.counter;
+  P.err = g.err;
+  P.V = static_cast<int>(g.V);
+  P.n_pb = static_cast<int>(ceil_div(g.V, kPB));
+  P.bkey = g.bkey;
+  P.tau = g.tau;
+  P.cnt = g.cnt;
+  P.cand = g.cand;
+  P.cap = g.cap;
+  cudaError_t e = cudaMemsetAsync(g.counter, 0, sizeof(uint32_t), s);
+  if (e != cudaSuccess) return e;
+  return pass == 1 ? launch_mode<kModeTopkMax>(P, g.num_sms, s)
+                   : launch_mode<kModeTopkCand>(P, g.num_sms, s);
 }
 
 }  // namespace kd

@@ -1,0 +1,294 @@
+// kd_topk_cache.cu -- building the offline teacher top-K cache: the row
+// kernels (per-row threshold and final selection) and the host entry point.
+//
+// The method keeps only the teacher's top 100 predictions per position
+// ("Efficient Knowledge Distillation for LLMs: Offline Top-K Logits and a
+// Fused Chunked KL Loss", ai2day.live story, "What did the researchers
+// change?").  Like the loss, the cache is built without the N x V logit grid:
+// per chunk of positions the tensor cores compute z = h_c W^T twice, tile by
+// tile, and only O(chunk * (V / 128 + 128 K)) numbers are kept.
+//
+// Every logit is compared through a 64-bit rank key (kd_tc_gemm.cu,
+// rank_key): the high word orders the float, the low word makes the lower
+// vocabulary index win among equal logits, so all keys of a row are distinct.
+// Pass 1 stores each 128-column block's largest key.  The row's threshold tau
+// is its K-th largest block key: exactly K blocks reach tau, so at least K
+// logits do, and every key >= tau lies in one of those K blocks -- at most
+// 128 K candidates whatever the data (ties included).  Pass 2 recomputes the
+// same tiles (same kernel, same accumulation order: bit-identical logits) and
+// appends the keys >= tau; the selection then takes the K largest.
+#include <string.h>
+
+#include <algorithm>
+
+#include "kd_internal.h"
+#include "kd_ptx.cuh"
+#include "kd_topk_cache.h"
+
+namespace kd {
+namespace {
+
+constexpr int kSelThreads = 256;
+
+__device__ __forceinline__ float key_value(uint64_t k) {
+  const uint32_t o = static_cast<uint32_t>(k >> 32);
+  if (o == 0u) return __uint_as_float(0x7FC00000u);  // NaN
+  const uint32_t u = (o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o;
+  return __uint_as_float(u);
+}
+
+__device__ __forceinline__ int32_t key_index(uint64_t k) {
+  return static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(k));
+}
+
+// The k-th largest (1-based) of n distinct 64-bit keys keys[0 .. n), by
+// radix selection on 8-bit digits from the most significant one.  Called by
+// every thread of the block; returns the same key to all of them.
+__device__ uint64_t kth_largest(const uint64_t* __restrict__ keys, int64_t n, int64_t k) {
+  __shared__ uint32_t hist[256];
+  __shared__ uint64_t s_prefix;
+  __shared__ int64_t s_k;
+  uint64_t prefix = 0, mask = 0;
+  if (threadIdx.x == 0) s_k = k;
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    for (int b = threadIdx.x; b < 256; b += blockDim.x) hist[b] = 0u;
+    __syncthreads();
+    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
+      const uint64_t key = keys[i];
+      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int64_t kk = s_k;
+      int b = 255;
+      for (; b > 0; --b) {
+        if (static_cast<int64_t>(hist[b]) >= kk) break;
+        kk -= hist[b];
+      }
+      s_k = kk;
+      s_prefix = prefix | (static_cast<uint64_t>(b) << shift);
+    }
+    __syncthreads();
+    prefix = s_prefix;
+    mask |= static_cast<uint64_t>(255u) << shift;
+  }
+  return prefix;
+}
+
+// tau[i] = the K-th largest block key of row i (0 -- below every key -- when
+// the row has fewer than K blocks, so that every logit is a candidate).
+__global__ void __launch_bounds__(kSelThreads) threshold_kernel(const uint64_t* __restrict__ bkey,
+                                                                int64_t n_pb, int64_t K,
+                                                                uint64_t* __restrict__ tau) {
+  const int64_t i = blockIdx.x;
+  uint64_t t = 0;
+  if (K <= n_pb) t = kth_largest(bkey + i * n_pb, n_pb, K);
+  if (threadIdx.x == 0) tau[i] = t;
+}
+
+// The K largest candidate keys of row i, sorted, decoded into (index, logit).
+__global__ void __launch_bounds__(kSelThreads) select_kernel(
+    const uint64_t* __restrict__ cand, int64_t cap, const uint32_t* __restrict__ cnt, int K,
+    int P2, int32_t* __restrict__ out_idx, float* __restrict__ out_val,
+    uint32_t* __restrict__ err) {
+  extern __shared__ uint64_t skey[];
+  __shared__ int s_n;
+  const int64_t i = blockIdx.x;
+  int64_t c = cnt[i];
+  if (c > cap) c = cap;  // cannot happen (the candidates are bounded by 128 K)
+  const uint64_t* row = cand + i * cap;
+  const uint64_t kth = c >= K ? kth_largest(row, c, K) : 0;
+  if (threadIdx.x == 0) s_n = 0;
+  for (int j = threadIdx.x; j < P2; j += blockDim.x) skey[j] = 0;
+  __syncthreads();
+  for (int64_t j = threadIdx.x; j < c; j += blockDim.x) {
+    const uint64_t key = row[j];
+    if (key >= kth) {
+      const int pos = atomicAdd(&s_n, 1);
+      if (pos < K) skey[pos] = key;
+    }
+  }
+  __syncthreads();
+  // bitonic sort, descending
+  for (int size = 2; size <= P2; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int j = threadIdx.x; j < P2; j += blockDim.x) {
+        const int o = j ^ stride;
+        if (o > j) {
+          const bool desc = (j & size) == 0;
+          const uint64_t a = skey[j], b = skey[o];
+          if ((a < b) == desc) {
+            skey[j] = b;
+            skey[o] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  bool nan_seen = false;
+  for (int j = threadIdx.x; j < K; j += blockDim.x) {
+    const uint64_t key = skey[j];
+    out_idx[i * K + j] = key_index(key);
+    out_val[i * K + j] = key_value(key);
+    nan_seen |= (key >> 32) == 0;
+  }
+  if (nan_seen) atomicOr(err, KD_FLAG_BAD_TEACHER);
+  if (threadIdx.x == 0 && s_n != K) atomicOr(err, KD_FLAG_INTERNAL);
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct CachePlan {
+  int64_t chunk, n_pb, cap;
+  size_t off_ctrl, off_bkey, off_tau, off_cnt, off_cand, off_sched, total;
+};
+
+bool valid_sizes(int64_t N, int64_t d, int64_t V, int32_t K) {
+  return N >= 0 && d >= 1 && V >= 1 && K >= 1 && K <= V;
+}
+
+kd_status cache_plan(int64_t N, int64_t d, int64_t V, int32_t K, int64_t chunk, CachePlan* p) {
+  if (!valid_sizes(N, d, V, K)) return KD_ERR_INVALID_ARG;
+  if (K > KD_MAX_K || d % 8 != 0) return KD_ERR_UNSUPPORTED;
+  if (N >= (int64_t(1) << 31) || V >= (int64_t(1) << 31) - 1024 || d >= (int64_t(1) << 24))
+    return KD_ERR_UNSUPPORTED;
+  p->n_pb = ceil_div(V, kPB);
+  p->cap = std::min<int64_t>(int64_t(kPB) * K, p->n_pb * kPB);
+  int64_t c = chunk > 0 ? chunk : kd_topk_cache_default_chunk(N, V, K);
+  if (N > 0 && c > N) c = N;
+  if (c < 1) c = 1;
+  if (c >= (int64_t(1) << 30)) return KD_ERR_UNSUPPORTED;
+  p->chunk = c;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align256(o + bytes);
+    return at;
+  };
+  const size_t cs = static_cast<size_t>(c);
+  p->off_ctrl = take(256);
+  p->off_bkey = take(8 * cs * static_cast<size_t>(p->n_pb));
+  p->off_tau = take(8 * cs);
+  p->off_cnt = take(4 * cs);
+  p->off_cand = take(8 * cs * static_cast<size_t>(p->cap));
+  p->off_sched = take(256);
+  p->total = o;
+  return KD_OK;
+}
+
+int num_sms_now() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+#define KD_CUDA(x)                              \
+  do {                                          \
+    if ((x) != cudaSuccess) return KD_ERR_CUDA; \
+  } while (0)
+
+}  // namespace
+}  // namespace kd
+
+extern "C" {
+
+int64_t kd_topk_cache_default_chunk(int64_t N, int64_t V, int32_t K) {
+  if (V < 1 || K < 1) return kd::kBM;
+  // About 2 GiB of per-chunk buffers; equal chunks, multiples of 128 rows.
+  const int64_t n_pb = kd::ceil_div(V, kd::kPB);
+  const int64_t cap = std::min<int64_t>(int64_t(kd::kPB) * K, n_pb * kd::kPB);
+  const int64_t per_row = 8 * (n_pb + cap + 1) + 4;
+  int64_t cmax = (int64_t(2) << 30) / per_row;
+  cmax = cmax / kd::kBM * kd::kBM;
+  if (cmax < kd::kBM) cmax = kd::kBM;
+  if (cmax > 16384) cmax = 16384;
+  const int64_t n = N < 1 ? 1 : N;
+  const int64_t pieces = kd::ceil_div(n, cmax);
+  return kd::round_up(kd::ceil_div(n, pieces), kd::kBM);
+}
+
+size_t kd_topk_cache_workspace_bytes(int64_t N, int64_t d, int64_t V, int32_t K, int64_t chunk) {
+  kd::CachePlan p;
+  if (kd::cache_plan(N, d, V, K, chunk, &p) != KD_OK) return 0;
+  return p.total;
+}
+
+kd_status kd_topk_cache_build(const void* h, const void* W, int64_t N, int64_t d, int64_t V,
+                              int32_t K, int64_t chunk, int32_t* topk_idx, float* topk_logit,
+                              void* workspace, size_t ws_bytes, uint32_t* dev_err_flags,
+                              cudaStream_t stream) {
+  kd::CachePlan P;
+  const kd_status st = kd::cache_plan(N, d, V, K, chunk, &P);
+  if (st != KD_OK) return st;
+  if (W == nullptr) return KD_ERR_INVALID_ARG;
+  if (N > 0 && (h == nullptr || topk_idx == nullptr || topk_logit == nullptr))
+    return KD_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(W) & 15u) != 0 ||
+      (N > 0 && (reinterpret_cast<uintptr_t>(h) & 15u) != 0))
+    return KD_ERR_INVALID_ARG;
+  if (workspace == nullptr || ws_bytes < P.total) return KD_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KD_ERR_WORKSPACE;
+  if (N == 0) return KD_OK;
+  const int sms = kd::num_sms_now();
+  if (sms <= 0) return KD_ERR_CUDA;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* err = dev_err_flags != nullptr ? dev_err_flags : reinterpret_cast<uint32_t*>(ws + P.off_ctrl);
+  uint64_t* bkey = reinterpret_cast<uint64_t*>(ws + P.off_bkey);
+  uint64_t* tau = reinterpret_cast<uint64_t*>(ws + P.off_tau);
+  uint32_t* cnt = reinterpret_cast<uint32_t*>(ws + P.off_cnt);
+  uint64_t* cand = reinterpret_cast<uint64_t*>(ws + P.off_cand);
+  uint32_t* sched = reinterpret_cast<uint32_t*>(ws + P.off_sched);
+  if (dev_err_flags == nullptr) KD_CUDA(cudaMemsetAsync(err, 0, sizeof(uint32_t), stream));
+
+  int P2 = 1;
+  while (P2 < K) P2 <<= 1;
+  const size_t sel_smem = static_cast<size_t>(P2) * sizeof(uint64_t);
+  KD_CUDA(cudaFuncSetAttribute(kd::select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(sel_smem)));
+
+  for (int64_t row0 = 0; row0 < N; row0 += P.chunk) {
+    const int64_t count = std::min<int64_t>(P.chunk, N - row0);
+    kd::TopkGemmArgs g;
+    memset(&g, 0, sizeof(g));
+    g.h = static_cast<const uint8_t*>(h) + row0 * d * 2;
+    g.W = W;
+    g.count = count;
+    g.d = d;
+    g.V = V;
+    g.bkey = bkey;
+    g.tau = tau;
+    g.cnt = cnt;
+    g.cand = cand;
+    g.cap = P.cap;
+    g.counter = sched;
+    g.err = err;
+    g.num_sms = sms;
+    {
+      kd::TimedLaunch tl(kd::kTopkBlockMax, stream);
+      KD_CUDA(kd::launch_tc_topk(g, 1, stream));
+    }
+    {
+      kd::TimedLaunch tl(kd::kTopkThreshold, stream);
+      kd::threshold_kernel<<<static_cast<unsigned>(count), kd::kSelThreads, 0, stream>>>(
+          bkey, P.n_pb, K, tau);
+      KD_CUDA(cudaGetLastError());
+    }
+    KD_CUDA(cudaMemsetAsync(cnt, 0, sizeof(uint32_t) * static_cast<size_t>(count), stream));
+    {
+      kd::TimedLaunch tl(kd::kTopkCandidates, stream);
+      KD_CUDA(kd::launch_tc_topk(g, 2, stream));
+    }
+    {
+      kd::TimedLaunch tl(kd::kTopkSelect, stream);
+      kd::select_kernel<<<static_cast<unsigned>(count), kd::kSelThreads, sel_smem, stream>>>(
+          cand, P.cap, cnt, K, P2, topk_idx + row0 * K, topk_logit + row0 * K, err);
+      KD_CUDA(cudaGetLastError());
+    }
+  }
+  return KD_OK;
+}
+
+}  // extern "C"
