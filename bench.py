@@ -222,6 +222,126 @@ def max_over_ranks(ms: float, world: int, device) -> float:
     return float(t.item())
 
 
+BUILDER_METRIC = "teacher top-K cache build tokens/s and TFLOP/s (% of B300 bf16 peak)"
+
+
+def run_builder(args):
+    """The offline teacher top-K cache (kd_topk_cache_build) on one GPU: the
+    workload's h as teacher final hidden states, its W as the teacher LM head
+    (d = 2880, V = 201,088 by default: a gpt-oss-120b-class teacher head), K
+    entries per position.  One step builds the cache of all N positions.  The
+    metric counts the logits' 2 N d V flops; the kernels execute 4 N d V (the
+    logits are computed twice, see include/kd_topk_cache.h)."""
+    import torch
+    import top_kl_loss_token_b300 as kd
+    from top_kl_loss_token_b300 import synth
+    kd.load_library()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    c = dict(synth.CONFIGS[args.config])
+    if args.tokens:
+        c["N"] = args.tokens
+    c["mask"] = None
+    c.pop("mask_frac_range", None)
+    x = synth.make_inputs(**c)
+    N, d, V, K = x.N, x.d, x.V, x.K
+    h_pin = torch.from_numpy(x.h.view(np.int16)).view(torch.bfloat16).pin_memory()
+    W = torch.from_numpy(x.W.view(np.int16)).view(torch.bfloat16).to(dev)
+    h = h_pin.to(dev)
+    chunk = args.chunk or int(kd.load_library().kd_topk_cache_default_chunk(N, V, K))
+    idx = torch.empty((N, K), dtype=torch.int32, device=dev)
+    val = torch.empty((N, K), dtype=torch.float32, device=dev)
+    ws = torch.empty(kd.topk_cache_workspace_bytes(N, d, V, K, chunk), dtype=torch.uint8, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kd.topk_cache_build(h, W, K, chunk, topk_idx=idx, topk_logit=val, workspace=ws,
+                            err_flags=err, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error flags {int(err.item())}")
+    kd.timing_enable(True)
+    kd.timing_collect()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    kd.timing_enable(False)
+    kernels = kd.timing_collect()
+    ms = ev0.elapsed_time(ev1)
+    value = N * args.steps / (ms / 1000.0)
+    peaks, peaks_src = load_peaks()
+    tflops = 2.0 * N * d * V * args.steps / (ms / 1000.0) / 1e12
+    dom = max(kernels.items(), key=lambda kv: kv[1][1])[0]
+    launches, tot_ms = kernels[dom]
+    flops_per_launch = 2.0 * N * d * V * args.steps / launches
+    achieved = flops_per_launch / (tot_ms / launches / 1000.0) / 1e12
+    roof = {"kernel": dom, "bound": "tensor", "achieved": achieved,
+            "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+            "frac": achieved / peaks["bf16_tflops_sustained"], "traffic": None,
+            "peak_source": f"{peaks_src} bf16 sustained (kernel timed inside a long step)",
+            "flops_per_launch": flops_per_launch, "avg_launch_ms": tot_ms / launches}
+    # end to end: teacher hidden states in from pinned memory, the cache out
+    idx_host = torch.empty((N, K), dtype=torch.int32).pin_memory()
+    val_host = torch.empty((N, K), dtype=torch.float32).pin_memory()
+    e_steps = max(1, min(args.steps, 5))
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        h.copy_(h_pin, non_blocking=True)
+        step()
+        idx_host.copy_(idx, non_blocking=True)
+        val_host.copy_(val, non_blocking=True)
+        stream.synchronize()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e_value = N * e_steps / (e0.elapsed_time(e1) / 1000.0)
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        rows = min(64, N)
+        hh = x.h_f32()[:rows].astype(np.float64)
+        WW = x.W_f32().astype(np.float64)
+        t0 = time.perf_counter()
+        oracle.topk_cache(hh, WW, K, block_rows=rows)
+        dtc = time.perf_counter() - t0
+        cpu = {"value": rows / dtc, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"fp64 oracle top-{K} cache of the first {rows} of {N} positions "
+                         f"({dtc:.1f} s)"}
+    line = {
+        "metric": BUILDER_METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"teacher top-{K} cache: N={N} positions, d={d}, V={V}, bf16 "
+                               f"hidden states and LM head", "chunk": chunk,
+                   "l2": "inputs larger than L2 (W alone 1.16 GB), no flush"},
+        "tflops_per_gpu": tflops, "tflops_executed_per_gpu": 2.0 * tflops,
+        "pct_of_bf16_peak": {"burst": tflops / peaks["bf16_tflops"],
+                             "sustained": tflops / peaks["bf16_tflops_sustained"],
+                             "source": peaks_src},
+        "workspace_gib": ws.numel() / 2 ** 30,
+        "roofline": roof, "cpu_baseline": cpu,
+        "e2e": {"value": e_value, "unit": "tokens/s", "h2d_bytes_per_step": h_pin.numel() * 2,
+                "d2h_bytes_per_step": N * K * 8},
+        "gpu_launches": sum(v[0] for v in kernels.values()),
+        "kernels": {k: {"launches": v[0], "ms": v[1]} for k, v in kernels.items()},
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_mem_scaling(args):
     """Device memory of one fused fwd+bwd at the 201,088-vocabulary shapes for
     N = 8K, 32K and 128K tokens at a fixed 8192-token chunk.  Extra memory (the
@@ -273,6 +393,9 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=64,
                     help="tokens per step of the reference (oracle) arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--builder", action="store_true",
+                    help="time the teacher top-K cache builder on the workload's teacher-side "
+                         "shapes instead of the loss")
     ap.add_argument("--mem-scaling", action="store_true",
                     help="report device memory at N = 8K, 32K, 128K tokens (fixed chunk) and exit")
     args = ap.parse_args()
@@ -297,6 +420,9 @@ def main():
 
     if args.mem_scaling:
         run_mem_scaling(args)
+        return
+    if args.builder:
+        run_builder(args)
         return
 
     if world > 1:
