@@ -74,6 +74,23 @@ kd_status kd_umma_gemm_bf16(const void* A, const void* B, float* D, int64_t M, i
                             uint32_t* counter, uint32_t* dev_err_flags, cudaStream_t stream);
 
 /*
+ * Test of the time-bounded waits (the write-ups define no counterpart).  Runs
+ * the kd_umma_gemm_bf16 kernel (A [M, K], B [N, K], both K-major) with one
+ * barrier arrival deliberately never made: the first operand stage of the
+ * first tile is never announced, so the MMA's wait for it cannot complete.
+ * Every wait of the kernel is limited to wait_limit_us microseconds; the wait
+ * that runs out raises KD_FLAG_TIMEOUT in *dev_err_flags, tells every other
+ * role of both CTAs of the pair to stop, lets in-flight copies and MMAs
+ * finish, frees the tensor memory and returns -- the context stays usable.
+ * D is left partly written.  Nothing faults or hangs: the call shows that a
+ * protocol error ends the kernel with a status the host can read.
+ */
+kd_status kd_umma_gemm_bf16_wait_test(const void* A, const void* B, float* D, int64_t M,
+                                      int64_t N, int64_t K, uint32_t wait_limit_us,
+                                      uint32_t* counter, uint32_t* dev_err_flags,
+                                      cudaStream_t stream);
+
+/*
  * Kernel timing (instrumentation; the write-ups define no counterpart).  While
  * enabled, the library brackets each of its kernel launches with a pair of
  * CUDA events recorded on the launching stream.  kd_timing_collect waits for

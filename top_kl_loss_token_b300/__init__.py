@@ -37,7 +37,7 @@ EXPORTS = ["kd_topk_kl_workspace_bytes", "kd_topk_kl_default_chunk", "kd_topk_kl
            "kd_topk_kl_fwd", "kd_status_string", "kd_topk_kl_workspace_layout",
            "kd_umma_gemm_bf16", "kd_timing_enable", "kd_timing_collect",
            "kd_topk_kl_fwd_bwd_noalloc", "kd_topk_cache_workspace_bytes",
-           "kd_topk_cache_default_chunk", "kd_topk_cache_build"]
+           "kd_topk_cache_default_chunk", "kd_topk_cache_build", "kd_umma_gemm_bf16_wait_test"]
 
 # Size of the library-held scratch array used by kd_topk_kl_fwd_bwd_noalloc.
 KD_NOALLOC_SCRATCH_BYTES = 64 << 20
@@ -101,6 +101,9 @@ def load_library(path: str = LIB_PATH):
     lib.kd_umma_gemm_bf16.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.c_int, ctypes.c_int,
                                       ctypes.c_int, vp, vp, vp]
     lib.kd_umma_gemm_bf16.restype = ctypes.c_int
+    lib.kd_umma_gemm_bf16_wait_test.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.c_uint32, vp, vp,
+                                                vp]
+    lib.kd_umma_gemm_bf16_wait_test.restype = ctypes.c_int
     lib.kd_timing_enable.argtypes = [ctypes.c_int]
     lib.kd_timing_enable.restype = ctypes.c_int
     lib.kd_timing_collect.argtypes = [ctypes.POINTER(TimingEntry), i32, ctypes.POINTER(i32)]

@@ -513,6 +513,46 @@ kd_status kd_umma_gemm_bf16(const void* A, const void* B, float* D, int64_t M, i
   return kd::launch_tc_gemm(g, stream) == cudaSuccess ? KD_OK : KD_ERR_CUDA;
 }
 
+kd_status kd_umma_gemm_bf16_wait_test(const void* A, const void* B, float* D, int64_t M,
+                                      int64_t N, int64_t K, uint32_t wait_limit_us,
+                                      uint32_t* counter, uint32_t* dev_err_flags,
+                                      cudaStream_t stream) {
+  if (A == nullptr || B == nullptr || D == nullptr || counter == nullptr ||
+      dev_err_flags == nullptr || wait_limit_us == 0)
+    return KD_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1) return KD_ERR_INVALID_ARG;
+  if (M >= (int64_t(1) << 30) || N >= (int64_t(1) << 30) || K >= (int64_t(1) << 30) || K % 8 != 0)
+    return KD_ERR_UNSUPPORTED;
+  if (!kd::aligned16(A) || !kd::aligned16(B)) return KD_ERR_INVALID_ARG;
+  if (kd::encode_fn() == nullptr) return KD_ERR_CUDA;
+  const int sms = kd::num_sms();
+  if (sms <= 0) return KD_ERR_CUDA;
+  kd::TcGemmArgs g;
+  memset(&g, 0, sizeof(g));
+  kd::TcProblem& p = g.pr[0];
+  p.A = A;
+  p.a_inner = K;
+  p.a_outer = M;
+  p.lda = K;
+  p.B = B;
+  p.b_inner = K;
+  p.b_outer = N;
+  p.ldb = K;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.out = D;
+  p.ldo = N;
+  g.nprob = 1;
+  g.chunk = static_cast<int>(M);
+  g.counter = counter;
+  g.err = dev_err_flags;
+  g.num_sms = sms;
+  g.wait_limit_ns = static_cast<uint64_t>(wait_limit_us) * 1000ull;
+  g.withhold_arrival = 1;
+  return kd::launch_tc_gemm(g, stream) == cudaSuccess ? KD_OK : KD_ERR_CUDA;
+}
+
 kd_status kd_timing_enable(int on) {
   kd::g_timing_on = on != 0;
   return KD_OK;

@@ -192,6 +192,8 @@ struct TcGemmArgs {
   uint32_t* counter;
   uint32_t* err;
   int num_sms;
+  uint64_t wait_limit_ns;  // 0: the default limit of every wait (4 s)
+  int withhold_arrival;    // test of the bounded waits only (kd_umma_gemm_bf16_wait_test)
 };
 cudaError_t launch_tc_gemm(const TcGemmArgs& g, cudaStream_t s);
 

@@ -68,6 +68,7 @@ struct WaitCtx {
   volatile int* abort;  // shared memory: set once any wait of the CTA timed out
   uint32_t peer_abort;  // shared::cluster address of the other CTA's flag (0: none)
   uint32_t* err;        // global error-flag word
+  uint64_t limit_ns;    // time limit of one wait
 };
 
 // Waits for the phase of `bar` with the given parity to complete.  Returns
@@ -81,7 +82,7 @@ static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, co
     if (mbar_try_wait(a, parity)) return true;
     if ((it & 15u) == 0) {
       if (*w.abort) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > w.limit_ns) {
         *w.abort = 1;
         if (w.peer_abort != 0u)
           asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(w.peer_abort), "r"(1u) : "memory");

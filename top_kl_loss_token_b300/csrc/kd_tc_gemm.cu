@@ -117,6 +117,8 @@ struct KParams {
   int chunk;
   uint32_t* counter;
   uint32_t* err;
+  uint64_t wait_limit_ns;  // 0: the default limit
+  int withhold_arrival;    // test of the bounded waits: never announce stage 0's bytes
   // pass-1 epilogue
   float k2;
   int V;
@@ -266,6 +268,7 @@ __device__ void producer_loop(const KParams& P, const Sizes& S, uint8_t* smem, C
   int slot = 0;
   uint32_t sphase = 0;
   bool aborted = false;
+  bool first_tile = true;
   const bool ring_head = (OPERAND == 0) && rank == 0;
   while (true) {
     int t;
@@ -310,7 +313,8 @@ __device__ void producer_loop(const KParams& P, const Sizes& S, uint8_t* smem, C
       }
       // Both CTAs' copies of A and B complete on the first CTA's barrier,
       // which expects the bytes of all four.
-      if (OPERAND == 0 && rank == 0) mbar_arrive_expect_tx(&ctl->full[stage], tx);
+      if (OPERAND == 0 && rank == 0 && !(P.withhold_arrival && kb == 0 && first_tile))
+        mbar_arrive_expect_tx(&ctl->full[stage], tx);
       const uint32_t fb = mapa_shared(smem_u32(&ctl->full[stage]), 0);
       uint8_t* dst = smem + stage * kStageBytes + (OPERAND == 0 ? 0 : kABytes);
       load_operand(dst, m, mode, fb, mn0, mn_count, kb * kBK);
@@ -319,6 +323,7 @@ __device__ void producer_loop(const KParams& P, const Sizes& S, uint8_t* smem, C
         phase ^= 1u;
       }
     }
+    first_tile = false;
     if (aborted) break;
   }
   if (aborted) {
@@ -782,7 +787,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
-  const WaitCtx wc{&ctl->abort, mapa_shared(smem_u32(&ctl->abort), rank ^ 1u), P.err};
+  const WaitCtx wc{&ctl->abort, mapa_shared(smem_u32(&ctl->abort), rank ^ 1u), P.err,
+                   P.wait_limit_ns != 0 ? P.wait_limit_ns : kWaitLimitNs};
 
   if (warp == 0) {
     if (lane == 0) producer_loop<MODE, 0>(P, S, smem, ctl, wc, rank);
@@ -915,6 +921,8 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& g, cudaStream_t s) {
   P.chunk = g.chunk;
   P.counter = g.counter;
   P.err = g.err;
+  P.wait_limit_ns = g.wait_limit_ns;
+  P.withhold_arrival = g.withhold_arrival;
   cudaError_t e = cudaMemsetAsync(g.counter, 0, sizeof(uint32_t), s);
   if (e != cudaSuccess) return e;
   return launch_mode<kModeStore>(P, g.num_sms, s);
