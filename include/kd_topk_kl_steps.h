@@ -60,6 +60,15 @@ kd_status kd_topk_kl_workspace_layout(int64_t N, int64_t d, int64_t V, int32_t K
                                       kd_dtype dtype, kd_workspace_layout* out);
 
 /*
+ * The same layout for a kd_full_kl_fwd_bwd call (kd_full_kl.h): ctrl, rows,
+ * lse (of the student's s) and loss_rows as above; the regions that belong to
+ * the top-K cache (sorted teacher entries, plogp, psum, part_ps, boff) do not
+ * exist there and are reported as offset 0.
+ */
+kd_status kd_full_kl_workspace_layout(int64_t N, int64_t d_s, int64_t d_t, int64_t V,
+                                      int64_t chunk, kd_workspace_layout* out);
+
+/*
  * D[M, N] (fp32, row-major, leading dimension N) = sum_k A(m, k) * B(n, k) on
  * the tcgen05 tensor cores, bf16 inputs, fp32 accumulation; D += ... when
  * accumulate != 0.

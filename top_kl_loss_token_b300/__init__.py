@@ -37,7 +37,9 @@ EXPORTS = ["kd_topk_kl_workspace_bytes", "kd_topk_kl_default_chunk", "kd_topk_kl
            "kd_topk_kl_fwd", "kd_status_string", "kd_topk_kl_workspace_layout",
            "kd_umma_gemm_bf16", "kd_timing_enable", "kd_timing_collect",
            "kd_topk_kl_fwd_bwd_noalloc", "kd_topk_cache_workspace_bytes",
-           "kd_topk_cache_default_chunk", "kd_topk_cache_build", "kd_umma_gemm_bf16_wait_test"]
+           "kd_topk_cache_default_chunk", "kd_topk_cache_build", "kd_umma_gemm_bf16_wait_test",
+           "kd_full_kl_workspace_bytes", "kd_full_kl_default_chunk", "kd_full_kl_fwd_bwd",
+           "kd_full_kl_workspace_layout"]
 
 # Size of the library-held scratch array used by kd_topk_kl_fwd_bwd_noalloc.
 KD_NOALLOC_SCRATCH_BYTES = 64 << 20
@@ -96,6 +98,16 @@ def load_library(path: str = LIB_PATH):
     lib.kd_topk_cache_default_chunk.restype = i64
     lib.kd_topk_cache_build.argtypes = [vp, vp, i64, i64, i64, i32, i64, vp, vp, vp, sz, vp, vp]
     lib.kd_topk_cache_build.restype = ctypes.c_int
+    lib.kd_full_kl_workspace_bytes.argtypes = [i64, i64, i64, i64, i64]
+    lib.kd_full_kl_workspace_bytes.restype = sz
+    lib.kd_full_kl_default_chunk.argtypes = [i64, i64]
+    lib.kd_full_kl_default_chunk.restype = i64
+    lib.kd_full_kl_workspace_layout.argtypes = [i64, i64, i64, i64, i64,
+                                                ctypes.POINTER(WorkspaceLayout)]
+    lib.kd_full_kl_workspace_layout.restype = ctypes.c_int
+    lib.kd_full_kl_fwd_bwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, f32, i64, vp, vp,
+                                       vp, vp, sz, vp, vp]
+    lib.kd_full_kl_fwd_bwd.restype = ctypes.c_int
     lib.kd_status_string.argtypes = [ctypes.c_int]
     lib.kd_status_string.restype = ctypes.c_char_p
     lib.kd_umma_gemm_bf16.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.c_int, ctypes.c_int,
@@ -283,6 +295,56 @@ def kd_topk_cache_build(h, W, K: int, chunk: int = 0, topk_idx=None, topk_logit=
     return topk_idx, topk_logit, workspace
 
 
+def full_kl_workspace_bytes(N: int, d_s: int, d_t: int, V: int, chunk: int = 0) -> int:
+    n = load_library().kd_full_kl_workspace_bytes(N, d_s, d_t, V, chunk)
+    if n == 0:
+        raise KDError(1, "kd_full_kl_workspace_bytes")
+    return int(n)
+
+
+def full_kl_workspace_layout(N: int, d_s: int, d_t: int, V: int, chunk: int = 0) -> WorkspaceLayout:
+    lay = WorkspaceLayout()
+    _check(load_library().kd_full_kl_workspace_layout(N, d_s, d_t, V, chunk, ctypes.byref(lay)),
+           "kd_full_kl_workspace_layout")
+    return lay
+
+
+def kd_full_kl_fwd_bwd(h_s, W_s, h_t, W_t, mask=None, T: float = 1.0, chunk: int = 0, loss=None,
+                       grad_h=None, grad_W=None, workspace=None, err_flags=None, stream=None):
+    """Full-vocabulary (K = V) distillation loss with the teacher computed in the
+    same pass (see include/kd_full_kl.h).  bf16 inputs.  Returns (loss [1],
+    grad_h [N, d_s], grad_W [V, d_s], workspace); asynchronous."""
+    import torch
+    for name, t in (("h_s", h_s), ("W_s", W_s), ("h_t", h_t), ("W_t", W_t)):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be a contiguous bfloat16 CUDA tensor")
+    N, d_s = h_s.shape
+    V, d_s2 = W_s.shape
+    N2, d_t = h_t.shape
+    V2, d_t2 = W_t.shape
+    if d_s2 != d_s or d_t2 != d_t or N2 != N or V2 != V:
+        raise ValueError("shape mismatch")
+    if mask is not None and (mask.dtype != torch.uint8 or not mask.is_cuda
+                             or not mask.is_contiguous() or mask.shape != (N,)):
+        raise TypeError("mask must be a contiguous uint8 CUDA tensor of shape [N]")
+    dev = h_s.device
+    if loss is None:
+        loss = torch.empty(1, dtype=torch.float32, device=dev)
+    if grad_h is None:
+        grad_h = torch.empty((N, d_s), dtype=torch.float32, device=dev)
+    if grad_W is None:
+        grad_W = torch.empty((V, d_s), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(full_kl_workspace_bytes(N, d_s, d_t, V, chunk), dtype=torch.uint8,
+                                device=dev)
+    st = load_library().kd_full_kl_fwd_bwd(
+        _ptr(h_s), _ptr(W_s), _ptr(h_t), _ptr(W_t), _ptr(mask), N, d_s, d_t, V, float(T),
+        int(chunk), _ptr(loss), _ptr(grad_h), _ptr(grad_W), _ptr(workspace), workspace.numel(),
+        _ptr(err_flags), _stream_handle(stream))
+    _check(st, "kd_full_kl_fwd_bwd")
+    return loss, grad_h, grad_W, workspace
+
+
 def kd_umma_gemm_bf16(A, B, M: int, N: int, K: int, a_mn_major: bool, b_mn_major: bool,
                       out=None, accumulate: bool = False, err_flags=None, stream=None):
     """D[M, N] (+)= A(m, k) B(n, k) on the tensor cores (see kd_topk_kl_steps.h)."""
@@ -361,5 +423,6 @@ fwd_bwd = kd_topk_kl_fwd_bwd
 fwd = kd_topk_kl_fwd
 fwd_bwd_noalloc = kd_topk_kl_fwd_bwd_noalloc
 topk_cache_build = kd_topk_cache_build
+full_kl_fwd_bwd = kd_full_kl_fwd_bwd
 timing_enable = kd_timing_enable
 timing_collect = kd_timing_collect

@@ -16,7 +16,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libkd_topk_kl.so")
-SOURCES = ["kd_api.cu", "kd_rowops.cu", "kd_tc_gemm.cu", "kd_noalloc.cu", "kd_topk_cache.cu"]
+SOURCES = ["kd_api.cu", "kd_rowops.cu", "kd_tc_gemm.cu", "kd_noalloc.cu", "kd_topk_cache.cu",
+           "kd_full_kl.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "-I" + INCLUDE]
 

@@ -54,7 +54,8 @@ const char* const kKindNames[kNumKinds] = {
     "teacher_prep", "compact",    "zero_invalid_rows", "gather_rows", "bucket_offsets",
     "pass1_gemm",   "lse_combine", "grad_tile",        "bwd_gemm",    "finalize",
     "simt_pass1",   "simt_gemm",   "topk_block_max",   "topk_threshold",
-    "topk_candidates", "topk_select"};
+    "topk_candidates", "topk_select", "mask_rows", "full_pass1_gemm", "full_lse_combine",
+    "full_grad_tile"};
 
 struct TimingRec {
   int kind;
@@ -198,6 +199,63 @@ kd_status make_plan(int64_t N, int64_t d, int64_t V, int32_t K, int64_t chunk, k
   return KD_OK;
 }
 
+cudaError_t launch_backward_gemms(const void* G, const void* W, const void* hc, int64_t d,
+                                  int64_t V, int64_t cpad, int64_t ldg, int64_t chunk,
+                                  const ChunkArgs& a, float* grad_h, float* grad_W,
+                                  int accumulate, uint32_t* counter, uint32_t* err, int sms,
+                                  cudaStream_t stream) {
+  TcGemmArgs g;
+  memset(&g, 0, sizeof(g));
+  TcProblem& gh = g.pr[0];  // grad_h rows of the chunk = G_c W
+  gh.A = G;
+  gh.a_mn = 0;
+  gh.a_inner = V;
+  gh.a_outer = cpad;
+  gh.lda = ldg;
+  gh.B = W;
+  gh.b_mn = 1;
+  gh.b_inner = d;
+  gh.b_outer = V;
+  gh.ldb = d;
+  gh.M = chunk;
+  gh.N = d;
+  gh.K = V;
+  gh.out = grad_h;
+  gh.ldo = d;
+  gh.row_map = a.rows;
+  gh.row_map_off = a.row0;
+  gh.accumulate = 0;
+  gh.count_mode = 1;
+  TcProblem& gw = g.pr[1];  // grad_W (+)= G_c^T h_c
+  gw.A = G;
+  gw.a_mn = 1;
+  // G's columns V .. ldg are zero, so whole 64-column atoms may be read
+  gw.a_inner = round_up(V, 64);
+  gw.a_outer = cpad;
+  gw.lda = ldg;
+  gw.B = hc;
+  gw.b_mn = 1;
+  gw.b_inner = d;
+  gw.b_outer = cpad;
+  gw.ldb = d;
+  gw.M = V;
+  gw.N = d;
+  gw.K = chunk;
+  gw.out = grad_W;
+  gw.ldo = d;
+  gw.row_map = nullptr;
+  gw.accumulate = accumulate;
+  gw.count_mode = 2;
+  g.nprob = 2;
+  g.n_valid = a.n_valid;
+  g.row0 = a.row0;
+  g.chunk = a.chunk;
+  g.counter = counter;
+  g.err = err;
+  g.num_sms = sms;
+  return launch_tc_gemm(g, stream);
+}
+
 namespace {
 
 struct Views {
@@ -330,56 +388,9 @@ kd_status run(const void* h, const void* W, kd_dtype dtype, const int32_t* topk_
     if (!want_grads) continue;
     KD_LAUNCH(kGradTile, launch_grad_tile(a, v.g, P.elem, T, stream));
     if (dtype == KD_BF16) {
-      TcGemmArgs g;
-      memset(&g, 0, sizeof(g));
-      TcProblem& gh = g.pr[0];  // grad_h rows of the chunk = G_c W
-      gh.A = v.g;
-      gh.a_mn = 0;
-      gh.a_inner = V;
-      gh.a_outer = P.cpad;
-      gh.lda = P.ldg;
-      gh.B = W;
-      gh.b_mn = 1;
-      gh.b_inner = d;
-      gh.b_outer = V;
-      gh.ldb = d;
-      gh.M = P.chunk;
-      gh.N = d;
-      gh.K = V;
-      gh.out = grad_h;
-      gh.ldo = d;
-      gh.row_map = v.rows;
-      gh.row_map_off = a.row0;
-      gh.accumulate = 0;
-      gh.count_mode = 1;
-      TcProblem& gw = g.pr[1];  // grad_W (+)= G_c^T h_c
-      gw.A = v.g;
-      gw.a_mn = 1;
-      // G's columns V .. ldg are zero, so whole 64-column atoms may be read
-      gw.a_inner = round_up(V, 64);
-      gw.a_outer = P.cpad;
-      gw.lda = P.ldg;
-      gw.B = v.hc;
-      gw.b_mn = 1;
-      gw.b_inner = d;
-      gw.b_outer = P.cpad;
-      gw.ldb = d;
-      gw.M = V;
-      gw.N = d;
-      gw.K = P.chunk;
-      gw.out = grad_W;
-      gw.ldo = d;
-      gw.row_map = nullptr;
-      gw.accumulate = j > 0 ? 1 : 0;
-      gw.count_mode = 2;
-      g.nprob = 2;
-      g.n_valid = a.n_valid;
-      g.row0 = a.row0;
-      g.chunk = a.chunk;
-      g.counter = v.sched + 1;
-      g.err = err;
-      g.num_sms = sms;
-      KD_LAUNCH(kBwdGemm, launch_tc_gemm(g, stream));
+      KD_LAUNCH(kBwdGemm, launch_backward_gemms(v.g, W, v.hc, d, V, P.cpad, P.ldg, P.chunk, a,
+                                                grad_h, grad_W, j > 0 ? 1 : 0, v.sched + 1, err,
+                                                sms, stream));
     } else {
       const float* G = static_cast<const float*>(v.g);
       SimtGemm gh;

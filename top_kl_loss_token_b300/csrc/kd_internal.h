@@ -44,6 +44,10 @@ enum KernelKind {
   kTopkThreshold,
   kTopkCandidates,
   kTopkSelect,
+  kMaskRows,
+  kFullPass1Gemm,
+  kFullLseCombine,
+  kFullGradTile,
   kNumKinds
 };
 
@@ -112,6 +116,14 @@ cudaError_t launch_grad_tile(const ChunkArgs& a, void* g, size_t elem, float T, 
 cudaError_t launch_finalize(const float* loss_rows, Ctrl* ctrl, float* loss, cudaStream_t s);
 cudaError_t launch_zero_invalid_rows(const int32_t* row_ok, int64_t N, int64_t d, float* grad_h,
                                      cudaStream_t s);
+
+// full-vocabulary loss
+cudaError_t launch_mask_rows(const uint8_t* mask, int64_t N, int32_t* row_ok, cudaStream_t s);
+cudaError_t launch_lse_dual(const ChunkArgs& a, float* part_mt, const float* part_lt,
+                            const float* part_a, float T, float* lse, float* loss_rows,
+                            cudaStream_t s);
+cudaError_t launch_grad_tile_dual(const ChunkArgs& a, const float* alpha_t, const uint16_t* u_t,
+                                  uint16_t* g, cudaStream_t s);
 
 // ----------------------------------------------------------- fp32 CUDA-core path
 cudaError_t launch_simt_pass1(const float* hc, const float* W, int64_t d, const ChunkArgs& a,
@@ -196,6 +208,36 @@ struct TcGemmArgs {
   int withhold_arrival;    // test of the bounded waits only (kd_umma_gemm_bf16_wait_test)
 };
 cudaError_t launch_tc_gemm(const TcGemmArgs& g, cudaStream_t s);
+
+// The backward of one chunk in one launch: grad_h rows of the chunk = G_c W
+// (stored through the compacted row map) and grad_W (+)= G_c^T h_c.
+// G [cpad, ldg] bf16, W [V, d] bf16, hc [cpad, d] bf16.
+cudaError_t launch_backward_gemms(const void* G, const void* W, const void* hc, int64_t d,
+                                  int64_t V, int64_t cpad, int64_t ldg, int64_t chunk,
+                                  const ChunkArgs& a, float* grad_h, float* grad_W,
+                                  int accumulate, uint32_t* counter, uint32_t* err, int sms,
+                                  cudaStream_t stream);
+
+// Full-vocabulary loss, pass 1 over one chunk: teacher and student logits of
+// each tile (problems 0 and 1 of one launch), their per-block statistics and
+// stored exponentials.
+struct DualPass1Args {
+  const void* hc_t;  // [cpad, d_t] bf16, the chunk's teacher hidden states
+  const void* W_t;   // [V, d_t] bf16
+  const void* hc_s;  // [cpad, d_s] bf16
+  const void* W_s;   // [V, d_s] bf16
+  int64_t d_t, d_s;
+  float k2;          // log2(e) / T
+  uint16_t* u_t;     // [cpad, ldg] bf16, written
+  uint16_t* u_s;     // [cpad, ldg] bf16, written
+  float* part_mt;    // [n_pb][cpad]
+  float* part_lt;
+  float* part_a;
+  uint32_t* counter;
+  uint32_t* err;
+  int num_sms;
+};
+cudaError_t launch_tc_dual_pass1(const DualPass1Args& p, const ChunkArgs& a, cudaStream_t s);
 
 // Teacher top-K cache: the two tensor-core passes over one chunk of positions
 // (z = h_c W^T).  pass 1 stores each 128-column block's largest rank key;

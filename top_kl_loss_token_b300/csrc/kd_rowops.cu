@@ -446,6 +446,138 @@ __global__ void __launch_bounds__(kGThreads) grad_tile_kernel(ChunkArgs a, E* __
   }
 }
 
+// ------------------------------------------------------------- full-vocabulary loss
+//
+// The teacher distribution is the softmax of the teacher's own logits over the
+// whole vocabulary (the pages' online-distillation setting, with nothing
+// discarded).  Per row, from the per-block statistics of pass 1 (base-2
+// units t2 = z_t log2(e) / T, s2 = z_s log2(e) / T):
+//   lse2_t = logsumexp2 of t2, lse2_s = logsumexp2 of s2,
+//   sum_v p_v (t2_v - s2_v) = sum_b 2^(m_t,b - lse2_t) a_b,
+//   loss_i = ln 2 * (sum_v p_v (t2_v - s2_v) - lse2_t + lse2_s),
+// and the factors that turn the stored exponentials into softmax / (T N_valid):
+//   alpha_s,b = 2^(m_s,b - lse2_s) / (T N_valid)   (over part_m)
+//   alpha_t,b = 2^(m_t,b - lse2_t) / (T N_valid)   (over part_mt).
+
+// row_ok[r] = mask[r] != 0 (every row when there is no mask).
+__global__ void mask_rows_kernel(const uint8_t* __restrict__ mask, int64_t N,
+                                 int32_t* __restrict__ row_ok) {
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (r < N) row_ok[r] = (mask == nullptr || mask[r] != 0) ? 1 : 0;
+}
+
+__device__ __forceinline__ void merge_block(float m, float l, float a, float& M, float& L,
+                                            float& A) {
+  if (m > M) {
+    const float f = ex2_approx(M - m);
+    L = L * f + l;
+    A = A * f + a;
+    M = m;
+  } else if (m > -INFINITY) {
+    const float f = ex2_approx(m - M);
+    L += l * f;
+    A += a * f;
+  }
+}
+
+__global__ void __launch_bounds__(kLseRows * kLseGroups) lse_dual_kernel(
+    ChunkArgs a, float* __restrict__ part_mt, const float* __restrict__ part_lt,
+    const float* __restrict__ part_a, float T, float* __restrict__ lse_out,
+    float* __restrict__ loss_rows) {
+  __shared__ float sMt[kLseGroups][kLseRows], sLt[kLseGroups][kLseRows], sA[kLseGroups][kLseRows];
+  __shared__ float sMs[kLseGroups][kLseRows], sLs[kLseGroups][kLseRows];
+  __shared__ float sLseT[kLseRows], sLseS[kLseRows];
+  const int count = chunk_count(a.n_valid, a.row0, a.chunk);
+  const int i0 = blockIdx.x * kLseRows;
+  if (i0 >= count) return;
+  const int x = threadIdx.x, y = threadIdx.y;
+  const int i = i0 + x;
+  const bool live = i < count;
+  float Mt = -INFINITY, Lt = 0.f, At = 0.f, Ms = -INFINITY, Ls = 0.f, dummy = 0.f;
+  if (live) {
+    for (int pb = y; pb < a.n_pb; pb += kLseGroups) {
+      const int64_t o = static_cast<int64_t>(pb) * a.cpad + i;
+      merge_block(part_mt[o], part_lt[o], part_a[o], Mt, Lt, At);
+      merge_block(a.part_m[o], a.part_l[o], 0.f, Ms, Ls, dummy);
+    }
+  }
+  sMt[y][x] = Mt;
+  sLt[y][x] = Lt;
+  sA[y][x] = At;
+  sMs[y][x] = Ms;
+  sLs[y][x] = Ls;
+  __syncthreads();
+  if (y == 0 && live) {
+    float MT = -INFINITY, LT = 0.f, AT = 0.f, MS = -INFINITY, LS = 0.f;
+    for (int g = 0; g < kLseGroups; ++g) {
+      merge_block(sMt[g][x], sLt[g][x], sA[g][x], MT, LT, AT);
+      merge_block(sMs[g][x], sLs[g][x], 0.f, MS, LS, dummy);
+    }
+    const float lse2_t = MT + lg2_approx(LT);
+    const float lse2_s = MS + lg2_approx(LS);
+    const float cross = AT / LT;  // sum_v p_v (t2_v - s2_v)
+    loss_rows[a.row0 + i] = kLn2 * (cross - lse2_t + lse2_s);
+    lse_out[a.row0 + i] = lse2_s * kLn2;
+    sLseT[x] = lse2_t;
+    sLseS[x] = lse2_s;
+  }
+  __syncthreads();
+  if (!live) return;
+  const float lse2_t = sLseT[x], lse2_s = sLseS[x];
+  const float scale = 1.0f / (T * static_cast<float>(*a.n_valid));
+  for (int pb = y; pb < a.n_pb; pb += kLseGroups) {
+    const int64_t o = static_cast<int64_t>(pb) * a.cpad + i;
+    a.part_m[o] = ex2_approx(a.part_m[o] - lse2_s) * scale;
+    part_mt[o] = ex2_approx(part_mt[o] - lse2_t) * scale;
+  }
+}
+
+// G[i, v] = u_s[i, v] * alpha_s,b - u_t[i, v] * alpha_t,b (b = v / 128), bf16,
+// written over u_s.  Rows count .. round_up(count, 64) and columns >= V are
+// zeroed (the grad_W reduction reads whole 64-row blocks).
+__global__ void __launch_bounds__(kGThreads) grad_tile_dual_kernel(
+    ChunkArgs a, const float* __restrict__ alpha_t, const uint16_t* __restrict__ u_t,
+    uint16_t* __restrict__ g) {
+  constexpr int W = 8;
+  extern __shared__ float sal[];
+  float* sas = sal;
+  float* sat = sal + a.n_pb;
+  const int count = chunk_count(a.n_valid, a.row0, a.chunk);
+  const int i = blockIdx.x;
+  if (i >= round_up(count, 64)) return;
+  uint16_t* row = g + static_cast<int64_t>(i) * a.ldg;
+  if (i >= count) {
+    float z[W];
+#pragma unroll
+    for (int j = 0; j < W; ++j) z[j] = 0.f;
+    for (int64_t v0 = static_cast<int64_t>(threadIdx.x) * W; v0 < a.ldg; v0 += kGThreads * W)
+      GVec<uint16_t>::store(row + v0, z);
+    return;
+  }
+  for (int pb = threadIdx.x; pb < a.n_pb; pb += kGThreads) {
+    sas[pb] = a.part_m[static_cast<int64_t>(pb) * a.cpad + i];
+    sat[pb] = alpha_t[static_cast<int64_t>(pb) * a.cpad + i];
+  }
+  __syncthreads();
+  const uint16_t* trow = u_t + static_cast<int64_t>(i) * a.ldg;
+  for (int64_t v0 = static_cast<int64_t>(threadIdx.x) * W; v0 < a.ldg; v0 += kGThreads * W) {
+    float f[W];
+    if (v0 >= a.V) {
+#pragma unroll
+      for (int j = 0; j < W; ++j) f[j] = 0.f;
+    } else {
+      const int pb = static_cast<int>(v0 / kPB);
+      const float as = sas[pb], at = sat[pb];
+      float ft[W];
+      GVec<uint16_t>::load(row + v0, f);
+      GVec<uint16_t>::load(trow + v0, ft);
+#pragma unroll
+      for (int j = 0; j < W; ++j) f[j] = (v0 + j < a.V) ? fmaf(f[j], as, -ft[j] * at) : 0.f;
+    }
+    GVec<uint16_t>::store(row + v0, f);
+  }
+}
+
 // loss = (sum of the per-row terms, in fixed order, in fp64) / N_valid.
 constexpr int kFinThreads = 1024;
 
@@ -732,6 +864,33 @@ cudaError_t launch_simt_gemm(const SimtGemm& g, cudaStream_t s) {
                   static_cast<unsigned>(ceil_div(g.M_cap, kGT)));
   if (grid.x == 0 || grid.y == 0) return cudaSuccess;
   simt_gemm_kernel<<<grid, 256, 0, s>>>(g);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mask_rows(const uint8_t* mask, int64_t N, int32_t* row_ok, cudaStream_t s) {
+  if (N == 0) return cudaSuccess;
+  mask_rows_kernel<<<static_cast<unsigned>(ceil_div(N, 256)), 256, 0, s>>>(mask, N, row_ok);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lse_dual(const ChunkArgs& a, float* part_mt, const float* part_lt,
+                            const float* part_a, float T, float* lse, float* loss_rows,
+                            cudaStream_t s) {
+  const dim3 block(kLseRows, kLseGroups);
+  lse_dual_kernel<<<static_cast<unsigned>(ceil_div(a.chunk, kLseRows)), block, 0, s>>>(
+      a, part_mt, part_lt, part_a, T, lse, loss_rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_grad_tile_dual(const ChunkArgs& a, const float* alpha_t, const uint16_t* u_t,
+                                  uint16_t* g, cudaStream_t s) {
+  const size_t smem = static_cast<size_t>(a.n_pb) * 8 + 16;
+  cudaError_t e = cudaFuncSetAttribute(grad_tile_dual_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem < 48 * 1024 ? 48 * 1024 : smem));
+  if (e != cudaSuccess) return e;
+  grad_tile_dual_kernel<<<static_cast<unsigned>(round_up(a.chunk, 64)), kGThreads, smem, s>>>(
+      a, alpha_t, u_t, g);
   return cudaGetLastError();
 }
 

@@ -94,7 +94,13 @@ enum : int {
   kLoadMN3d = 2   // MN-major, atom-aligned: one 3-D box covering every atom
 };
 
-enum : int { kModePass1 = 0, kModeStore = 1, kModeTopkMax = 2, kModeTopkCand = 3 };
+enum : int {
+  kModePass1 = 0,     // student logits + top-K statistics (the loss against the cache)
+  kModeStore = 1,     // plain GEMMs, fp32 results stored or accumulated
+  kModeTopkMax = 2,   // teacher top-K cache, pass 1
+  kModeTopkCand = 3,  // teacher top-K cache, pass 2
+  kModeDual = 4       // full-vocabulary loss: teacher then student logits of one tile
+};
 
 struct KParams {
   CUtensorMap tmA[2];
@@ -140,6 +146,12 @@ struct KParams {
   uint32_t* cnt;         // [count] candidates appended so far
   uint64_t* cand;        // [count][cap] candidate rank keys
   int64_t cap;
+  // full-vocabulary loss (kModeDual): problem 0 is the teacher, problem 1 the
+  // student; student statistics go to part_m / part_l and u
+  uint16_t* u_t;         // [cpad, ldg] teacher exponentials 2^(t2 - m_t), bf16
+  float* part_mt;        // [n_pb][cpad] teacher block max of t2
+  float* part_lt;        // [n_pb][cpad] teacher block sum of 2^(t2 - m_t)
+  float* part_a;         // [n_pb][cpad] block sum of 2^(t2 - m_t) (t2 - s2)
 };
 
 struct Sizes {
@@ -176,6 +188,10 @@ __device__ __forceinline__ Sizes get_sizes(const KParams& P) {
     s.tiles[pi] = tiles;
     s.total += tiles;
   }
+  if (P.u_t != nullptr) {  // full-vocabulary pass: one tile covers both problems
+    s.total = s.tiles[0];
+    s.tiles[1] = 0;
+  }
   return s;
 }
 
@@ -196,14 +212,14 @@ __device__ __forceinline__ Tile decode_tile(const Sizes& S, int t) {
     t -= S.tiles[0];
   }
   const int pi = tl.prob;
-  if (MODE == kModePass1 || MODE == kModeTopkMax || MODE == kModeTopkCand) {
+  if (MODE == kModePass1 || MODE == kModeTopkMax || MODE == kModeTopkCand || MODE == kModeDual) {
     tl.m = t % S.mt[pi];
     tl.n = t / S.mt[pi];
   } else {
     tl.n = t % S.nt[pi];
     tl.m = t / S.nt[pi];
   }
-  tl.nkb = S.nkb[pi];
+  tl.nkb = S.nkb[pi] + (MODE == kModeDual ? S.nkb[1] : 0);
   // The pair MMA takes B as two halves of n_cols / 2 columns, one from each
   // CTA; a 3-D loaded B half must start on a 64-column atom (n_cols a
   // multiple of 128), any other B half on 8 columns (n_cols a multiple of 16).
@@ -294,8 +310,8 @@ __device__ void producer_loop(const KParams& P, const Sizes& S, uint8_t* smem, C
     if (t < 0) break;
     const Tile tl = decode_tile<MODE>(S, t);
     const int pi = tl.prob;
-    const CUtensorMap* m = OPERAND == 0 ? &P.tmA[pi] : &P.tmB[pi];
-    const int mode = OPERAND == 0 ? P.a_load[pi] : P.b_load[pi];
+    // kModeDual: the first nkb[0] K blocks are the teacher's, then the student's
+    const int nkb0 = MODE == kModeDual ? S.nkb[0] : tl.nkb;
     int mn0, mn_count;
     if (OPERAND == 0) {
       mn0 = tl.m * kPairM + static_cast<int>(rank) * kBM;
@@ -314,10 +330,13 @@ __device__ void producer_loop(const KParams& P, const Sizes& S, uint8_t* smem, C
       // Both CTAs' copies of A and B complete on the first CTA's barrier,
       // which expects the bytes of all four.
       if (OPERAND == 0 && rank == 0 && !(P.withhold_arrival && kb == 0 && first_tile))
-        mbar_arrive_expect_tx(&ctl->full[stage], tx);
+        mbar_arrive_expect_tx(&ctl->full[stage], kb < nkb0 ? tx : P.tx_bytes[1]);
       const uint32_t fb = mapa_shared(smem_u32(&ctl->full[stage]), 0);
       uint8_t* dst = smem + stage * kStageBytes + (OPERAND == 0 ? 0 : kABytes);
-      load_operand(dst, m, mode, fb, mn0, mn_count, kb * kBK);
+      const int pk = kb < nkb0 ? pi : 1;
+      const CUtensorMap* m = OPERAND == 0 ? &P.tmA[pk] : &P.tmB[pk];
+      const int mode = OPERAND == 0 ? P.a_load[pk] : P.b_load[pk];
+      load_operand(dst, m, mode, fb, mn0, mn_count, (kb < nkb0 ? kb : kb - nkb0) * kBK);
       if (++stage == kStages) {
         stage = 0;
         phase ^= 1u;
@@ -356,12 +375,16 @@ __device__ void mma_loop(const KParams& P, const Sizes& S, uint8_t* smem, Ctl* c
     }
     if (t < 0) break;
     const Tile tl = decode_tile<MODE>(S, t);
-    const int b = it & 1;
-    const uint32_t tp = (static_cast<uint32_t>(it) >> 1) & 1u;
+    // kModeDual: one accumulator set per tile (teacher in columns 0-255,
+    // student in 256-511); otherwise two 256-column accumulators in turn.
+    const int b = MODE == kModeDual ? 0 : (it & 1);
+    const uint32_t tp = MODE == kModeDual ? (static_cast<uint32_t>(it) & 1u)
+                                          : ((static_cast<uint32_t>(it) >> 1) & 1u);
     ++it;
     if (!mbar_wait(&ctl->tempty[b], tp ^ 1u, wc)) break;
     tc_fence_after();
-    const uint32_t d_tmem = tmem + static_cast<uint32_t>(b * kBN);
+    const uint32_t d_tmem0 = tmem + static_cast<uint32_t>(b * kBN);
+    const int nkb0 = MODE == kModeDual ? S.nkb[0] : tl.nkb;
     const int pi = tl.prob;
     const int a_mn = P.a_mn[pi], b_mn = P.b_mn[pi];
     const uint32_t idesc = idesc_bf16_f32(kPairM, tl.n_cols, a_mn, b_mn);
@@ -374,6 +397,9 @@ __device__ void mma_loop(const KParams& P, const Sizes& S, uint8_t* smem, Ctl* c
       tc_fence_after();
       const uint32_t sa = smem_u32(smem + stage * kStageBytes);
       const uint32_t sb = sa + kABytes;
+      const bool second = kb >= nkb0;  // kModeDual: the student's K blocks
+      const uint32_t d_tmem = d_tmem0 + (second ? static_cast<uint32_t>(kBN) : 0u);
+      const int kb_in = second ? kb - nkb0 : kb;
 #pragma unroll
       for (int kk = 0; kk < kBK / 16; ++kk) {
         // K-major: the next 16 K elements are 32 bytes further along each
@@ -382,7 +408,7 @@ __device__ void mma_loop(const KParams& P, const Sizes& S, uint8_t* smem, Ctl* c
                                  : sdesc_sw128(sa + kk * 32, 16, 1024);
         const uint64_t bd = b_mn ? sdesc_sw128(sb + kk * 2048, kAtomBytes, 1024)
                                  : sdesc_sw128(sb + kk * 32, 16, 1024);
-        umma_bf16_pair(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+        umma_bf16_pair(d_tmem, ad, bd, idesc, (kb_in > 0 || kk > 0) ? 1u : 0u);
       }
       umma_commit_pair_both(&ctl->empty[stage]);
       if (++stage == kStages) {
@@ -739,6 +765,136 @@ __device__ void epilogue_topk(const KParams& P, const Sizes& S, Ctl* ctl, uint32
   }
 }
 
+// Full-vocabulary loss: maxima of 32 teacher and student logits (raw z).
+__device__ __forceinline__ void dual_max32(uint32_t ta_t, uint32_t ta_s, int nvalid, float& mt,
+                                           float& ms) {
+  float t[32], s[32];
+  tmem_ld_x32(ta_t, t);
+  tmem_ld_x32(ta_s, s);
+  tmem_ld_wait();
+  reg_fence(t);
+  reg_fence(s);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    if (j < nvalid) {
+      mt = fmaxf(mt, t[j]);
+      ms = fmaxf(ms, s[j]);
+    }
+  }
+}
+
+// Exponentials of 32 teacher and student logits relative to the block maxima
+// (base-2 units t2 = z_t k2, s2 = z_s k2), their sums, the teacher-weighted
+// difference sum of 2^(t2 - mt2) (t2 - s2), and both sets stored as bf16.
+__device__ __forceinline__ void dual_exp32(uint32_t ta_t, uint32_t ta_s, int nvalid, float k2,
+                                           float mt2, float ms2, float& lt, float& ls, float& a,
+                                           uint16_t* ut, uint16_t* us, bool store) {
+  float t[32], s[32];
+  tmem_ld_x32(ta_t, t);
+  tmem_ld_x32(ta_s, s);
+  tmem_ld_wait();
+  reg_fence(t);
+  reg_fence(s);
+  uint32_t wt[16], ws[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    float et[2], es[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int c = 2 * j + h;
+      const float t2 = t[c] * k2, s2 = s[c] * k2;
+      et[h] = 0.f;
+      es[h] = 0.f;
+      if (c < nvalid) {
+        et[h] = ex2_approx(t2 - mt2);
+        es[h] = ex2_approx(s2 - ms2);
+        lt += et[h];
+        ls += es[h];
+        a = fmaf(et[h], t2 - s2, a);
+      }
+    }
+    wt[j] = pack_bf16x2(et[0], et[1]);
+    ws[j] = pack_bf16x2(es[0], es[1]);
+  }
+  if (!store) return;
+  uint4* dt = reinterpret_cast<uint4*>(ut);
+  uint4* ds = reinterpret_cast<uint4*>(us);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    dt[j] = make_uint4(wt[4 * j], wt[4 * j + 1], wt[4 * j + 2], wt[4 * j + 3]);
+    ds[j] = make_uint4(ws[4 * j], ws[4 * j + 1], ws[4 * j + 2], ws[4 * j + 3]);
+  }
+}
+
+// Full-vocabulary loss epilogue.  The tile's teacher logits are in TMEM
+// columns 0-255 and the student's in 256-511; each thread owns one row and
+// one 128-column block: block maxima m_t, m_s (base 2), sums l_t, l_s, the
+// cross term a, and the stored exponentials of both.
+__device__ void epilogue_dual(const KParams& P, const Sizes& S, Ctl* ctl, uint32_t tmem,
+                              const WaitCtx& wc, int warp, int lane, int rank) {
+  const int q = warp & 3;
+  const int half = (warp - 2) >> 2;
+  int slot = 0;
+  uint32_t sphase = 0;
+  int it = 0;
+  const float k2 = P.k2;
+  while (true) {
+    int t = -1;
+    bool ok = sched_pop(ctl, slot, sphase, t, wc);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) break;
+    __syncwarp();
+    if (lane == 0) sched_release(ctl, slot);
+    if (++slot == kSched) {
+      slot = 0;
+      sphase ^= 1u;
+    }
+    if (t < 0) break;
+    const Tile tl = decode_tile<kModeDual>(S, t);
+    const uint32_t tp = static_cast<uint32_t>(it) & 1u;
+    ++it;
+    const int i = tl.m * kPairM + rank * kBM + q * 32 + lane;
+    const int col0 = tl.n * kBN + half * 128;
+    const int pb = tl.n * 2 + half;
+    const bool live = (i < S.count) && (pb < P.n_pb);
+    const int nv = min(128, P.V - col0);  // warp-uniform
+    ok = mbar_wait(&ctl->tfull[0], tp, wc);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) break;
+    tc_fence_after();
+    const uint32_t ta = tmem + (static_cast<uint32_t>(q * 32) << 16) +
+                        static_cast<uint32_t>(half * 128);
+    const uint32_t ts = ta + static_cast<uint32_t>(kBN);
+    float mt = -INFINITY, ms = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      if (nv > 32 * c) dual_max32(ta + 32 * c, ts + 32 * c, nv - 32 * c, mt, ms);
+    const float mt2 = mt * k2, ms2 = ms * k2;
+    float lt = 0.f, ls = 0.f, a = 0.f;
+    const int64_t urow = static_cast<int64_t>(live ? i : 0) * P.ldg + col0;
+    uint16_t* ut = P.u_t + urow;
+    uint16_t* us = P.u + urow;
+    // every lane takes part in the (warp-collective) TMEM loads; only rows of
+    // the chunk store
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      if (nv > 32 * c)
+        dual_exp32(ta + 32 * c, ts + 32 * c, nv - 32 * c, k2, mt2, ms2, lt, ls, a, ut + 32 * c,
+                   us + 32 * c, live);
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->tempty[0]), 0));
+    if (live) {
+      const int64_t o = static_cast<int64_t>(pb) * P.cpad + i;
+      P.part_mt[o] = mt2;
+      P.part_lt[o] = lt;
+      P.part_a[o] = a;
+      P.part_m[o] = ms2;
+      P.part_l[o] = ls;
+    }
+  }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ KParams P) {
   extern __shared__ uint8_t smem_raw[];
@@ -801,6 +957,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       epilogue_pass1(P, S, ctl, tmem, wc, warp, lane, static_cast<int>(rank));
     else if (MODE == kModeStore)
       epilogue_store(P, S, ctl, tmem, wc, warp, lane, static_cast<int>(rank));
+    else if (MODE == kModeDual)
+      epilogue_dual(P, S, ctl, tmem, wc, warp, lane, static_cast<int>(rank));
     else
       epilogue_topk<MODE>(P, S, ctl, tmem, wc, warp, lane, static_cast<int>(rank));
   }
@@ -966,6 +1124,48 @@ cudaError_t launch_tc_pass1(const Pass1Args& p, const ChunkArgs& a, cudaStream_t
   cudaError_t e = cudaMemsetAsync(p.counter, 0, sizeof(uint32_t), s);
   if (e != cudaSuccess) return e;
   return launch_mode<kModePass1>(P, p.num_sms, s);
+}
+
+cudaError_t launch_tc_dual_pass1(const DualPass1Args& p, const ChunkArgs& a, cudaStream_t s) {
+  KParams P;
+  memset(&P, 0, sizeof(P));
+  // problem 0: teacher logits h_t,c W_t^T; problem 1: student logits h_s,c W_s^T
+  if (!encode_operand(&P.tmA[0], p.hc_t, kLoadK, p.d_t, a.cpad, p.d_t, kBM) ||
+      !encode_operand(&P.tmB[0], p.W_t, kLoadK, p.d_t, a.V, p.d_t, kBN / 2) ||
+      !encode_operand(&P.tmA[1], p.hc_s, kLoadK, p.d_s, a.cpad, p.d_s, kBM) ||
+      !encode_operand(&P.tmB[1], p.W_s, kLoadK, p.d_s, a.V, p.d_s, kBN / 2))
+    return cudaErrorInvalidValue;
+  for (int pi = 0; pi < 2; ++pi) {
+    P.a_load[pi] = P.b_load[pi] = kLoadK;
+    P.M[pi] = a.chunk;
+    P.N[pi] = a.V;
+    P.bn[pi] = kBN;
+    P.tx_bytes[pi] = 2u * kStageBytes;
+    P.count_mode[pi] = 1;
+  }
+  P.K[0] = static_cast<int>(p.d_t);
+  P.K[1] = static_cast<int>(p.d_s);
+  P.nprob = 2;
+  P.n_valid = a.n_valid;
+  P.row0 = a.row0;
+  P.chunk = a.chunk;
+  P.counter = p.counter;
+  P.err = p.err;
+  P.k2 = p.k2;
+  P.V = a.V;
+  P.cpad = a.cpad;
+  P.n_pb = a.n_pb;
+  P.part_m = a.part_m;
+  P.part_l = a.part_l;
+  P.u = p.u_s;
+  P.ldg = a.ldg;
+  P.u_t = p.u_t;
+  P.part_mt = p.part_mt;
+  P.part_lt = p.part_lt;
+  P.part_a = p.part_a;
+  cudaError_t e = cudaMemsetAsync(p.counter, 0, sizeof(uint32_t), s);
+  if (e != cudaSuccess) return e;
+  return launch_mode<kModeDual>(P, p.num_sms, s);
 }
 
 cudaError_t launch_tc_topk(const TopkGemmArgs& g, int pass, cudaStream_t s) {
