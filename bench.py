@@ -342,6 +342,140 @@ def run_builder(args):
     print(json.dumps(line), flush=True)
 
 
+FULL_METRIC = "full-vocabulary KL fwd+bwd tokens/s and TFLOP/s (% of B300 bf16 peak)"
+
+
+def run_full_teacher(args):
+    """The full-vocabulary loss (kd_full_kl_fwd_bwd): the workload's student
+    (h, W) against a teacher of the same hidden size whose hidden states and
+    LM head are drawn like the student's from their own seed.  One step is one
+    fused fwd+bwd over all N tokens; it executes 2 N d_t V (teacher logits) +
+    6 N d_s V (student logits, grad_h, grad_W) flops."""
+    import torch
+    import top_kl_loss_token_b300 as kd
+    from top_kl_loss_token_b300 import synth
+    kd.load_library()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    c = dict(synth.CONFIGS[args.config])
+    if args.tokens:
+        c["N"] = args.tokens
+        if c.get("mask") == "packed":
+            c["mask_frac_range"] = None
+    xs = synth.make_inputs(**c)
+    ct = dict(c)
+    ct["seed"] = c["seed"] + 50
+    ct["mask"] = None
+    ct.pop("mask_frac_range", None)
+    ct["K"] = 1
+    xt = synth.make_inputs(**ct)
+    N, d, V = xs.N, xs.d, xs.V
+
+    def bf(a):
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    hs_pin, ht_pin = bf(xs.h).pin_memory(), bf(xt.h).pin_memory()
+    m_pin = None if xs.mask is None else torch.from_numpy(xs.mask).pin_memory()
+    Ws, Wt = bf(xs.W).to(dev), bf(xt.W).to(dev)
+    hs, ht = hs_pin.to(dev), ht_pin.to(dev)
+    mask = None if m_pin is None else m_pin.to(dev)
+    chunk = args.chunk or int(kd.load_library().kd_full_kl_default_chunk(N, V))
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    gh = torch.empty((N, d), dtype=torch.float32, device=dev)
+    gW = torch.empty((V, d), dtype=torch.float32, device=dev)
+    ws = torch.empty(kd.full_kl_workspace_bytes(N, d, d, V, chunk), dtype=torch.uint8, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kd.full_kl_fwd_bwd(hs, Ws, ht, Wt, mask, xs.T, chunk, loss=loss, grad_h=gh, grad_W=gW,
+                           workspace=ws, err_flags=err, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error flags {int(err.item())}")
+    kd.timing_enable(True)
+    kd.timing_collect()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    kd.timing_enable(False)
+    kernels = kd.timing_collect()
+    ms = ev0.elapsed_time(ev1)
+    value = N * args.steps / (ms / 1000.0)
+    valid = N if xs.mask is None else int(xs.mask.sum())
+    flops_step = 8.0 * N * d * V
+    tflops = flops_step * args.steps / (ms / 1000.0) / 1e12
+    peaks, peaks_src = load_peaks()
+    per_token = {"full_pass1_gemm": 4.0 * d * V, "bwd_gemm": 4.0 * d * V}
+    dom = max(kernels.items(), key=lambda kv: kv[1][1])[0]
+    roof = None
+    if dom in per_token:
+        launches, tot_ms = kernels[dom]
+        fpl = per_token[dom] * valid * args.steps / launches
+        ach = fpl / (tot_ms / launches / 1000.0) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": ach,
+                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": ach / peaks["bf16_tflops_sustained"], "traffic": None,
+                "peak_source": f"{peaks_src} bf16 sustained (kernel timed inside a long step)",
+                "flops_per_launch": fpl, "avg_launch_ms": tot_ms / launches}
+    loss_host = torch.empty(1, dtype=torch.float32).pin_memory()
+    h2d = 2 * hs_pin.numel() * 2 + (0 if m_pin is None else m_pin.numel())
+    e_steps = max(1, min(args.steps, 5))
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        hs.copy_(hs_pin, non_blocking=True)
+        ht.copy_(ht_pin, non_blocking=True)
+        if m_pin is not None:
+            mask.copy_(m_pin, non_blocking=True)
+        step()
+        loss_host.copy_(loss, non_blocking=True)
+        stream.synchronize()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e_value = N * e_steps / (e0.elapsed_time(e1) / 1000.0)
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        rows = min(64, N)
+        t0 = time.perf_counter()
+        oracle.full_kl_fwd_bwd(xs.h_f32()[:rows], xs.W_f32(), xt.h_f32()[:rows], xt.W_f32(),
+                               None if xs.mask is None else xs.mask[:rows], xs.T, block_rows=rows)
+        dtc = time.perf_counter() - t0
+        cpu = {"value": rows / dtc, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"fp64 oracle fwd+bwd of the first {rows} of {N} tokens ({dtc:.1f} s)"}
+    line = {
+        "metric": FULL_METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": workload_name(xs) + f"; teacher d={d} computed in the same pass",
+                   "chunk": chunk, "l2": "inputs larger than L2 (W alone 1.16 GB), no flush"},
+        "tflops_per_gpu": tflops,
+        "pct_of_bf16_peak": {"burst": tflops / peaks["bf16_tflops"],
+                             "sustained": tflops / peaks["bf16_tflops_sustained"],
+                             "source": peaks_src},
+        "workspace_gib": ws.numel() / 2 ** 30,
+        "roofline": roof, "cpu_baseline": cpu,
+        "e2e": {"value": e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": 4},
+        "gpu_launches": sum(v[0] for v in kernels.values()),
+        "kernels": {k: {"launches": v[0], "ms": v[1]} for k, v in kernels.items()},
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_mem_scaling(args):
     """Device memory of one fused fwd+bwd at the 201,088-vocabulary shapes for
     N = 8K, 32K and 128K tokens at a fixed 8192-token chunk.  Extra memory (the
@@ -396,6 +530,9 @@ def main():
     ap.add_argument("--builder", action="store_true",
                     help="time the teacher top-K cache builder on the workload's teacher-side "
                          "shapes instead of the loss")
+    ap.add_argument("--full-teacher", action="store_true",
+                    help="time the full-vocabulary loss with the teacher computed in the same "
+                         "pass (teacher hidden size = the student's) instead of the top-K loss")
     ap.add_argument("--mem-scaling", action="store_true",
                     help="report device memory at N = 8K, 32K, 128K tokens (fixed chunk) and exit")
     args = ap.parse_args()
@@ -423,6 +560,9 @@ def main():
         return
     if args.builder:
         run_builder(args)
+        return
+    if args.full_teacher:
+        run_full_teacher(args)
         return
 
     if world > 1:

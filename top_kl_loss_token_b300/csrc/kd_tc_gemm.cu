@@ -375,8 +375,11 @@ __device__ void mma_loop(const KParams& P, const Sizes& S, uint8_t* smem, Ctl* c
     }
     if (t < 0) break;
     const Tile tl = decode_tile<MODE>(S, t);
-    // kModeDual: one accumulator set per tile (teacher in columns 0-255,
-    // student in 256-511); otherwise two 256-column accumulators in turn.
+    // kModeDual: the teacher's accumulator is TMEM columns 0-255 (barriers
+    // tfull/tempty[0]) and the student's 256-511 (barriers [1]); the epilogue
+    // frees the teacher's as soon as it has copied it, so the next tile's
+    // teacher product overlaps the epilogue.  Otherwise: two 256-column
+    // accumulators used in turn.
     const int b = MODE == kModeDual ? 0 : (it & 1);
     const uint32_t tp = MODE == kModeDual ? (static_cast<uint32_t>(it) & 1u)
                                           : ((static_cast<uint32_t>(it) >> 1) & 1u);
@@ -390,6 +393,15 @@ __device__ void mma_loop(const KParams& P, const Sizes& S, uint8_t* smem, Ctl* c
     const uint32_t idesc = idesc_bf16_f32(kPairM, tl.n_cols, a_mn, b_mn);
     bool ok = true;
     for (int kb = 0; kb < tl.nkb; ++kb) {
+      if (MODE == kModeDual && kb == nkb0) {
+        // teacher product done; the student's accumulator must be free
+        umma_commit_pair_both(&ctl->tfull[0]);
+        if (!mbar_wait(&ctl->tempty[1], tp ^ 1u, wc)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
       if (!mbar_wait_fast(&ctl->full[stage], phase, wc)) {
         ok = false;
         break;
@@ -417,7 +429,7 @@ __device__ void mma_loop(const KParams& P, const Sizes& S, uint8_t* smem, Ctl* c
       }
     }
     if (!ok) break;
-    umma_commit_pair_both(&ctl->tfull[b]);
+    umma_commit_pair_both(&ctl->tfull[MODE == kModeDual ? 1 : b]);
   }
   // Every MMA this thread issued must finish before TMEM is freed.
   umma_commit_pair_local(&ctl->drain);
@@ -765,71 +777,66 @@ __device__ void epilogue_topk(const KParams& P, const Sizes& S, Ctl* ctl, uint32
   }
 }
 
-// Full-vocabulary loss: maxima of 32 teacher and student logits (raw z).
-__device__ __forceinline__ void dual_max32(uint32_t ta_t, uint32_t ta_s, int nvalid, float& mt,
-                                           float& ms) {
-  float t[32], s[32];
-  tmem_ld_x32(ta_t, t);
-  tmem_ld_x32(ta_s, s);
+// Full-vocabulary loss: maximum of up to 16 student logits (raw z) from TMEM.
+__device__ __forceinline__ float max16_tmem(uint32_t ta, int nvalid, float m) {
+  float s[16];
+  tmem_ld_x16(ta, s);
   tmem_ld_wait();
-  reg_fence(t);
   reg_fence(s);
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    if (j < nvalid) {
-      mt = fmaxf(mt, t[j]);
-      ms = fmaxf(ms, s[j]);
-    }
-  }
+  for (int j = 0; j < 16; ++j)
+    if (j < nvalid) m = fmaxf(m, s[j]);
+  return m;
 }
 
-// Exponentials of 32 teacher and student logits relative to the block maxima
-// (base-2 units t2 = z_t k2, s2 = z_s k2), their sums, the teacher-weighted
-// difference sum of 2^(t2 - mt2) (t2 - s2), and both sets stored as bf16.
-__device__ __forceinline__ void dual_exp32(uint32_t ta_t, uint32_t ta_s, int nvalid, float k2,
+// Exponentials of 16 teacher logits (registers) and 16 student logits (TMEM)
+// relative to the block maxima (base-2 units t2 = z_t k2, s2 = z_s k2), their
+// sums, the teacher-weighted difference sum of 2^(t2 - mt2) (t2 - s2), and
+// both sets stored as bf16 when `store`.
+__device__ __forceinline__ void dual_exp16(const float* t, uint32_t ta_s, int nvalid, float k2,
                                            float mt2, float ms2, float& lt, float& ls, float& a,
                                            uint16_t* ut, uint16_t* us, bool store) {
-  float t[32], s[32];
-  tmem_ld_x32(ta_t, t);
-  tmem_ld_x32(ta_s, s);
+  float s[16];
+  tmem_ld_x16(ta_s, s);
   tmem_ld_wait();
-  reg_fence(t);
   reg_fence(s);
-  uint32_t wt[16], ws[16];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    float et[2], es[2];
+  for (int g = 0; g < 2; ++g) {  // 8 columns at a time, stored as they are done
+    uint32_t wt[4], ws[4];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int c = 2 * j + h;
-      const float t2 = t[c] * k2, s2 = s[c] * k2;
-      et[h] = 0.f;
-      es[h] = 0.f;
-      if (c < nvalid) {
-        et[h] = ex2_approx(t2 - mt2);
-        es[h] = ex2_approx(s2 - ms2);
-        lt += et[h];
-        ls += es[h];
-        a = fmaf(et[h], t2 - s2, a);
+    for (int j = 0; j < 4; ++j) {
+      float et[2], es[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c = 8 * g + 2 * j + h;
+        const float t2 = t[c] * k2, s2 = s[c] * k2;
+        et[h] = 0.f;
+        es[h] = 0.f;
+        if (c < nvalid) {
+          et[h] = ex2_approx(t2 - mt2);
+          es[h] = ex2_approx(s2 - ms2);
+          lt += et[h];
+          ls += es[h];
+          a = fmaf(et[h], t2 - s2, a);
+        }
       }
+      wt[j] = pack_bf16x2(et[0], et[1]);
+      ws[j] = pack_bf16x2(es[0], es[1]);
     }
-    wt[j] = pack_bf16x2(et[0], et[1]);
-    ws[j] = pack_bf16x2(es[0], es[1]);
-  }
-  if (!store) return;
-  uint4* dt = reinterpret_cast<uint4*>(ut);
-  uint4* ds = reinterpret_cast<uint4*>(us);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    dt[j] = make_uint4(wt[4 * j], wt[4 * j + 1], wt[4 * j + 2], wt[4 * j + 3]);
-    ds[j] = make_uint4(ws[4 * j], ws[4 * j + 1], ws[4 * j + 2], ws[4 * j + 3]);
+    if (store) {
+      reinterpret_cast<uint4*>(ut)[g] = make_uint4(wt[0], wt[1], wt[2], wt[3]);
+      reinterpret_cast<uint4*>(us)[g] = make_uint4(ws[0], ws[1], ws[2], ws[3]);
+    }
   }
 }
 
 // Full-vocabulary loss epilogue.  The tile's teacher logits are in TMEM
 // columns 0-255 and the student's in 256-511; each thread owns one row and
-// one 128-column block: block maxima m_t, m_s (base 2), sums l_t, l_s, the
-// cross term a, and the stored exponentials of both.
+// one 128-column block.  It copies its 128 teacher logits into registers and
+// frees the teacher accumulator at once (the next tile's teacher product then
+// runs during the rest of this epilogue), then computes the block maxima
+// m_t, m_s (base 2), the sums l_t, l_s, the cross term a and the stored
+// exponentials of both from the registers and the student accumulator.
 __device__ void epilogue_dual(const KParams& P, const Sizes& S, Ctl* ctl, uint32_t tmem,
                               const WaitCtx& wc, int warp, int lane, int rank) {
   const int q = warp & 3;
@@ -838,6 +845,8 @@ __device__ void epilogue_dual(const KParams& P, const Sizes& S, Ctl* ctl, uint32
   uint32_t sphase = 0;
   int it = 0;
   const float k2 = P.k2;
+  const uint32_t tempty0 = mapa_shared(smem_u32(&ctl->tempty[0]), 0);
+  const uint32_t tempty1 = mapa_shared(smem_u32(&ctl->tempty[1]), 0);
   while (true) {
     int t = -1;
     bool ok = sched_pop(ctl, slot, sphase, t, wc);
@@ -858,17 +867,38 @@ __device__ void epilogue_dual(const KParams& P, const Sizes& S, Ctl* ctl, uint32
     const int pb = tl.n * 2 + half;
     const bool live = (i < S.count) && (pb < P.n_pb);
     const int nv = min(128, P.V - col0);  // warp-uniform
+    const uint32_t ta = tmem + (static_cast<uint32_t>(q * 32) << 16) +
+                        static_cast<uint32_t>(half * 128);
+    const uint32_t ts = ta + static_cast<uint32_t>(kBN);
+    // teacher logits -> registers, then free the teacher accumulator
     ok = mbar_wait(&ctl->tfull[0], tp, wc);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) break;
     tc_fence_after();
-    const uint32_t ta = tmem + (static_cast<uint32_t>(q * 32) << 16) +
-                        static_cast<uint32_t>(half * 128);
-    const uint32_t ts = ta + static_cast<uint32_t>(kBN);
-    float mt = -INFINITY, ms = -INFINITY;
+    float tv[128];
+    {
+      float (&t0)[32] = *reinterpret_cast<float(*)[32]>(tv);
+      float (&t1)[32] = *reinterpret_cast<float(*)[32]>(tv + 32);
+      float (&t2)[32] = *reinterpret_cast<float(*)[32]>(tv + 64);
+      float (&t3)[32] = *reinterpret_cast<float(*)[32]>(tv + 96);
+      load_acc128(ta, t0, t1, t2, t3);
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive_cluster(tempty0);
+    float mt = -INFINITY;
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
-      if (nv > 32 * c) dual_max32(ta + 32 * c, ts + 32 * c, nv - 32 * c, mt, ms);
+    for (int j = 0; j < 128; ++j)
+      if (j < nv) mt = fmaxf(mt, tv[j]);
+    // student logits: maximum, then exponentials together with the teacher's
+    ok = mbar_wait(&ctl->tfull[1], tp, wc);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) break;
+    tc_fence_after();
+    float ms = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      if (nv > 16 * c) ms = max16_tmem(ts + 16 * c, nv - 16 * c, ms);
     const float mt2 = mt * k2, ms2 = ms * k2;
     float lt = 0.f, ls = 0.f, a = 0.f;
     const int64_t urow = static_cast<int64_t>(live ? i : 0) * P.ldg + col0;
@@ -877,13 +907,13 @@ __device__ void epilogue_dual(const KParams& P, const Sizes& S, Ctl* ctl, uint32
     // every lane takes part in the (warp-collective) TMEM loads; only rows of
     // the chunk store
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
-      if (nv > 32 * c)
-        dual_exp32(ta + 32 * c, ts + 32 * c, nv - 32 * c, k2, mt2, ms2, lt, ls, a, ut + 32 * c,
-                   us + 32 * c, live);
+    for (int c = 0; c < 8; ++c)
+      if (nv > 16 * c)
+        dual_exp16(tv + 16 * c, ts + 16 * c, nv - 16 * c, k2, mt2, ms2, lt, ls, a, ut + 16 * c,
+                   us + 16 * c, live);
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->tempty[0]), 0));
+    if (lane == 0) mbar_arrive_cluster(tempty1);
     if (live) {
       const int64_t o = static_cast<int64_t>(pb) * P.cpad + i;
       P.part_mt[o] = mt2;
