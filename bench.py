@@ -459,7 +459,10 @@ def run_full_teacher(args):
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": workload_name(xs) + f"; teacher d={d} computed in the same pass",
+        "config": {"workload": (f"{xs.name} student: N={N} tokens, d={d}, V={V}, T={xs.T:g}, "
+                                f"bf16 h/W" + (f", {xs.masked_fraction() * 100:.1f}% masked"
+                                               if xs.mask is not None else "")
+                                + f"; full-vocabulary teacher d={d} computed in the same pass"),
                    "chunk": chunk, "l2": "inputs larger than L2 (W alone 1.16 GB), no flush"},
         "tflops_per_gpu": tflops,
         "pct_of_bf16_peak": {"burst": tflops / peaks["bf16_tflops"],
