@@ -128,3 +128,36 @@ def test_topk_cache_argument_errors_and_plan(lib):
     per_row = 8 * (128 * 100 + 1571 + 1) + 4
     assert 8192 * per_row <= n <= 8192 * per_row + 4096
     assert lib.kd_topk_cache_default_chunk(32768, 201088, 100) % 128 == 0
+
+
+def test_full_kl_argument_errors_and_plan(lib):
+    f = lib.kd_full_kl_fwd_bwd
+    ok = dict(hs=256, Ws=256, ht=256, Wt=256, mask=None, N=8, ds=16, dt=24, V=300, T=1.0,
+              chunk=0, loss=256, gh=256, gW=256, ws=256, ws_bytes=1 << 40)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return f(a["hs"], a["Ws"], a["ht"], a["Wt"], a["mask"], a["N"], a["ds"], a["dt"], a["V"],
+                 a["T"], a["chunk"], a["loss"], a["gh"], a["gW"], a["ws"], a["ws_bytes"], None, None)
+    for kw in (dict(Ws=None), dict(Wt=None), dict(hs=None), dict(ht=None), dict(loss=None),
+               dict(gh=None), dict(gW=None), dict(N=-1), dict(ds=0), dict(dt=0), dict(V=0),
+               dict(T=0.0), dict(T=float("nan")), dict(T=-2.0), dict(ht=264)):
+        assert call(**kw) == 1, kw
+    assert call(ds=12) == 2 and call(dt=20) == 2
+    assert call(ws=None) == 3 and call(ws_bytes=100) == 3
+    # extra memory is O(chunk V + N): both models' exponential tiles per chunk
+    a = kd.full_kl_workspace_bytes(32768, 2880, 2880, 201088, 8192)
+    b = kd.full_kl_workspace_bytes(131072, 2880, 2880, 201088, 8192)
+    assert b - a < (131072 - 32768) * 64
+    assert a < 2 * 8192 * 201216 * 2 * 1.2
+    lay = kd.full_kl_workspace_layout(32768, 2880, 2880, 201088, 8192)
+    assert lay.chunk == 8192 and lay.off_idx_sorted == 0 and lay.off_rows > 0
+    assert lib.kd_full_kl_default_chunk(32768, 201088) % 128 == 0
+
+
+def test_bounded_wait_test_entry_rejects_bad_arguments(lib):
+    f = lib.kd_umma_gemm_bf16_wait_test
+    assert f(None, 16, 16, 8, 8, 8, 1000, 16, 16, None) == 1
+    assert f(16, 16, 16, 8, 8, 8, 0, 16, 16, None) == 1      # a zero time limit
+    assert f(16, 16, 16, 8, 8, 12, 1000, 16, 16, None) == 2  # K % 8 != 0
