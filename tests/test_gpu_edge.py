@@ -1,0 +1,73 @@
+"""Edge cases of the CUDA paths against the fp64 oracle: bitwise determinism
+of repeated calls, extreme temperatures and logit magnitudes (the online
+logsumexp must not overflow), the smallest sizes (one token, d = 8, a
+one-word vocabulary), a vocabulary smaller than one tile, and one token per
+chunk."""
+import numpy as np
+import pytest
+
+import oracle
+from top_kl_loss_token_b300 import synth
+from kd_testutil import TOL, assert_parity, run_gpu, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(kd, x, chunk=0):
+    ref = oracle.fwd_bwd(x.h_f32(), x.W_f32(), x.idx, x.logit, x.mask, x.T)
+    got = run_gpu(kd, x, chunk)
+    assert got["err"] == 0
+    if ref["n_valid"] and abs(ref["loss"]) > 1e-9:
+        assert_parity(got, ref, x.dtype)
+    return got, ref
+
+
+def test_repeated_calls_are_bitwise_identical(kd):
+    import torch
+    x = synth.make_inputs(700, 256, 3000, 16, T=2.0, dtype="bf16", seed=301, mask="random0.1")
+    t = to_device(x)
+    a = run_gpu(kd, x, 256, tensors=t)
+    b = run_gpu(kd, x, 256, tensors=t)
+    assert a["loss"] == b["loss"]
+    np.testing.assert_array_equal(a["grad_h"], b["grad_h"])
+    np.testing.assert_array_equal(a["grad_W"], b["grad_W"])
+    # the cache builder and the full-vocabulary loss as well
+    h, W = t[0], t[1]
+    i1, v1, _ = kd.topk_cache_build(h, W, 20)
+    i2, v2, _ = kd.topk_cache_build(h, W, 20)
+    torch.cuda.synchronize()
+    assert torch.equal(i1, i2) and torch.equal(v1, v2)
+    l1, g1, w1, _ = kd.full_kl_fwd_bwd(h, W, h.flip(0).contiguous(), W, t[4], 1.3)
+    l2, g2, w2, _ = kd.full_kl_fwd_bwd(h, W, h.flip(0).contiguous(), W, t[4], 1.3)
+    torch.cuda.synchronize()
+    assert torch.equal(l1, l2) and torch.equal(g1, g2) and torch.equal(w1, w2)
+
+
+@pytest.mark.parametrize("T", [0.05, 50.0])
+def test_extreme_temperatures(kd, T):
+    x = synth.make_inputs(300, 128, 2000, 12, T=T, dtype="bf16", seed=302, mask="random0.1",
+                          w_std=0.1)
+    _check(kd, x, 128)
+
+
+def test_large_logits_do_not_overflow(kd):
+    # |z| up to ~300: exp(z) overflows fp32 without the running maximum
+    x = synth.make_inputs(260, 64, 1500, 8, T=1.0, dtype="bf16", seed=303, w_std=3.0)
+    x.logit = (x.logit * 20).astype(np.float32)
+    got, ref = _check(kd, x)
+    assert np.isfinite(got["grad_W"]).all() and np.isfinite(got["loss"])
+
+
+def test_one_token_one_word_vocabulary(kd):
+    # V = K = 1: p = q = 1, the loss and both gradients are exactly zero
+    x = synth.make_inputs(1, 8, 1, 1, T=1.0, dtype="bf16", seed=304)
+    got = run_gpu(kd, x)
+    assert got["err"] == 0 and got["loss"] == 0.0
+    assert np.all(got["grad_h"] == 0) and np.all(got["grad_W"] == 0)
+
+
+@pytest.mark.parametrize("N,d,V,K,chunk", [(1, 8, 300, 3, 0), (40, 16, 100, 5, 1),
+                                           (130, 8, 257, 4, 0)])
+def test_small_and_ragged_sizes(kd, N, d, V, K, chunk):
+    x = synth.make_inputs(N, d, V, K, T=1.0, dtype="bf16", seed=305 + N, w_std=0.2)
+    _check(kd, x, chunk)
