@@ -19,8 +19,6 @@ namespace kd {
 
 namespace {
 
-size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
-
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -39,15 +37,6 @@ EncodeTiledFn encode_fn() {
   });
   return fn;
 }
-
-int num_sms() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  return n;
-}
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // ------------------------------------------------------------- kernel timing
 const char* const kKindNames[kNumKinds] = {
@@ -299,18 +288,6 @@ Views views(const Plan& P, void* ws) {
   v.sched = reinterpret_cast<uint32_t*>(b + L.off_sched);
   return v;
 }
-
-#define KD_CUDA(x)                            \
-  do {                                        \
-    if ((x) != cudaSuccess) return KD_ERR_CUDA; \
-  } while (0)
-
-// A kernel launch (through its launch function) with optional timing.
-#define KD_LAUNCH(kind, x)              \
-  do {                                  \
-    TimedLaunch timed_launch_(kind, stream); \
-    KD_CUDA(x);                         \
-  } while (0)
 
 kd_status run(const void* h, const void* W, kd_dtype dtype, const int32_t* topk_idx,
               const float* topk_logit, const uint8_t* mask, int64_t N, int64_t d, int64_t V,

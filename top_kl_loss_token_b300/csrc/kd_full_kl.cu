@@ -17,8 +17,6 @@
 namespace kd {
 namespace {
 
-size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
-
 struct FullPlan {
   int64_t N, d_s, d_t, V, chunk, cpad, n_pb, ldg, n_chunks;
   size_t off_ctrl, off_row_ok, off_rows, off_lse, off_loss_rows, off_part_m, off_part_l,
@@ -72,26 +70,6 @@ kd_status full_plan(int64_t N, int64_t d_s, int64_t d_t, int64_t V, int64_t chun
   P.total = o;
   return KD_OK;
 }
-
-int sm_count() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  return n;
-}
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-#define KD_CUDA(x)                              \
-  do {                                          \
-    if ((x) != cudaSuccess) return KD_ERR_CUDA; \
-  } while (0)
-
-#define KD_LAUNCH(kind, x)                    \
-  do {                                        \
-    kd::TimedLaunch timed_launch_(kind, stream);  \
-    KD_CUDA(x);                               \
-  } while (0)
 
 }  // namespace
 }  // namespace kd
@@ -159,7 +137,7 @@ kd_status kd_full_kl_fwd_bwd(const void* h_s, const void* W_s, const void* h_t, 
     return KD_ERR_INVALID_ARG;
   if (workspace == nullptr || ws_bytes < P.total) return KD_ERR_WORKSPACE;
   if (!kd::aligned16(workspace)) return KD_ERR_WORKSPACE;
-  const int sms = kd::sm_count();
+  const int sms = kd::num_sms();
   if (sms <= 0) return KD_ERR_CUDA;
 
   uint8_t* b = static_cast<uint8_t*>(workspace);

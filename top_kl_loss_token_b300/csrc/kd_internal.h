@@ -26,6 +26,30 @@ constexpr int kNoIndex = 0x7fffffff;
 __host__ __device__ constexpr int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 __host__ __device__ constexpr int64_t ceil_div(int64_t x, int64_t m) { return (x + m - 1) / m; }
 
+// Host helpers shared by the entry points.
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// Streaming multiprocessors of the current device (0 on error).
+inline int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+// In host functions returning kd_status: a failed CUDA call returns
+// KD_ERR_CUDA; KD_LAUNCH also brackets the launch with the optional timing
+// events (needs a `stream` in scope).
+#define KD_CUDA(x)                                    \
+  do {                                                \
+    if ((x) != cudaSuccess) return KD_ERR_CUDA;       \
+  } while (0)
+#define KD_LAUNCH(kind, x)                            \
+  do {                                                \
+    ::kd::TimedLaunch timed_launch_(kind, stream);    \
+    KD_CUDA(x);                                       \
+  } while (0)
+
 // Kernel kinds, for the optional per-launch timing (kd_timing_enable).
 enum KernelKind {
   kTeacherPrep,

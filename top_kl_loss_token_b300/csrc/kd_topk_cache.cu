@@ -137,8 +137,6 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
   if (threadIdx.x == 0 && s_n != K) atomicOr(err, KD_FLAG_INTERNAL);
 }
 
-size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
-
 struct CachePlan {
   int64_t chunk, n_pb, cap;
   size_t off_ctrl, off_bkey, off_tau, off_cnt, off_cand, off_sched, total;
@@ -176,18 +174,6 @@ kd_status cache_plan(int64_t N, int64_t d, int64_t V, int32_t K, int64_t chunk, 
   p->total = o;
   return KD_OK;
 }
-
-int num_sms_now() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  return n;
-}
-
-#define KD_CUDA(x)                              \
-  do {                                          \
-    if ((x) != cudaSuccess) return KD_ERR_CUDA; \
-  } while (0)
 
 }  // namespace
 }  // namespace kd
@@ -231,7 +217,7 @@ kd_status kd_topk_cache_build(const void* h, const void* W, int64_t N, int64_t d
   if (workspace == nullptr || ws_bytes < P.total) return KD_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KD_ERR_WORKSPACE;
   if (N == 0) return KD_OK;
-  const int sms = kd::num_sms_now();
+  const int sms = kd::num_sms();
   if (sms <= 0) return KD_ERR_CUDA;
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
