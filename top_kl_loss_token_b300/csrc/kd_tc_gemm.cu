@@ -1,19 +1,27 @@
-// kd_tc_gemm.cu -- the tensor-core kernels of the fused top-K KL loss.
+// kd_tc_gemm.cu -- the tensor-core kernels of the fused top-K KL loss and of
+// the other paths built on it.
 //
-// One persistent, warp-specialised kernel template runs every contraction of
-// the loss on the tcgen05 tensor cores ("Efficient Knowledge Distillation for
-// LLMs: Offline Top-K Logits and a Fused Chunked KL Loss", ai2day.live story,
-// "What did the researchers change?": the student logits are produced and
-// consumed one chunk of the sequence at a time, never as the full grid):
+// One persistent, warp-specialised kernel template runs every contraction on
+// the tcgen05 tensor cores ("Efficient Knowledge Distillation for LLMs:
+// Offline Top-K Logits and a Fused Chunked KL Loss", ai2day.live story, "What
+// did the researchers change?": the logits are produced and consumed one chunk
+// of the sequence at a time, never as the full grid).  The launch modes:
 //
-//   pass 1   z = h_c W^T for one token chunk (M = chunk rows, N = V, K = d),
-//            with an epilogue that turns each 128 x 128 quarter of the fp32
-//            accumulator into logsumexp statistics (block max, sum of
-//            exponentials, teacher-weighted logit sum) and stores the
-//            normalised exponentials u = 2^(s2 - m2) as bf16;
-//   backward grad_h rows of the chunk = G_c W   (M = chunk, N = d, K = V) and
-//            grad_W (+)= G_c^T h_c              (M = V, N = d, K = chunk),
-//            both in the same launch, fp32 results stored or accumulated.
+//   pass 1     z = h_c W^T for one token chunk (M = chunk rows, N = V, K = d);
+//              the epilogue turns each 128 x 128 quarter of the fp32
+//              accumulator into logsumexp statistics (block max, sum of
+//              exponentials, teacher-weighted logit sum) and stores the
+//              normalised exponentials u = 2^(s2 - m2) as bf16;
+//   backward   grad_h rows of the chunk = G_c W   (M = chunk, N = d, K = V) and
+//              grad_W (+)= G_c^T h_c              (M = V, N = d, K = chunk),
+//              both in the same launch, fp32 results stored or accumulated
+//              (also the plain GEMM of kd_umma_gemm_bf16);
+//   top-K      the teacher top-K cache: the largest rank key of every
+//              128-column block (first pass), then the keys reaching each
+//              row's threshold (second pass);
+//   dual       the full-vocabulary loss: the teacher's and the student's
+//              logits of the same tile into the two accumulators, their block
+//              statistics and both sets of stored exponentials.
 //
 // The kernel runs as clusters of two CTAs ("CTA pairs", one CTA per SM).  A
 // pair owns a 256-row output tile: each CTA stages its 128 rows of A and half
@@ -23,7 +31,7 @@
 // operand bytes per stage, so 7 stages of 64-deep K blocks fit in shared
 // memory.
 //
-// CTA layout (320 threads):
+// CTA layout (352 threads):
 //   warp 0      TMA producer of A.  In the first CTA it also takes tile
 //               numbers from a global counter and hands them to every role of
 //               both CTAs through a shared-memory ring;
