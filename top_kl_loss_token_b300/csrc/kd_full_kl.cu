@@ -83,7 +83,7 @@ int64_t kd_full_kl_default_chunk(int64_t N, int64_t V) {
   int64_t cmax = (int64_t(8) << 30) / (4 * ldg);
   cmax = cmax / kd::kBM * kd::kBM;
   if (cmax < kd::kBM) cmax = kd::kBM;
-  if (cmax > 16384) cmax = 16384;
+  if (cmax > kd::kMaxChunk) cmax = kd::kMaxChunk;
   const int64_t n = N < 1 ? 1 : N;
   const int64_t pieces = kd::ceil_div(n, cmax);
   return kd::round_up(kd::ceil_div(n, pieces), kd::kBM);

@@ -18,6 +18,9 @@ namespace kd {
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
+// Largest default chunk, in tokens: its hidden states (re-read by every tile
+// of a launch) must stay resident in L2.
+constexpr int64_t kMaxChunk = 8192;
 // The logsumexp statistics are kept per 128-column block of the vocabulary.
 constexpr int kPB = 128;
 // A sorted-index slot that holds no entry (dropped, or padding).
