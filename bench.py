@@ -34,6 +34,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "fused KL fwd+bwd tokens/s and TFLOP/s (% of B300 bf16 peak); peak GiB"
+FWD_METRIC = "fused KL fwd (loss only) tokens/s and TFLOP/s (% of B300 bf16 peak)"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 
@@ -163,8 +164,9 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_oracle_time(x, rows: int):
-    """Times the fp64 oracle's fwd+bwd on the first `rows` tokens of x."""
+def cpu_oracle_time(x, rows: int, grads: bool = True):
+    """Times the fp64 oracle (fwd+bwd, or the loss alone) on the first `rows`
+    tokens of x."""
     import oracle
     try:
         from threadpoolctl import threadpool_info
@@ -175,7 +177,10 @@ def cpu_oracle_time(x, rows: int):
     W = x.W_f32().astype(np.float64)
     m = None if x.mask is None else x.mask[:rows]
     t0 = time.perf_counter()
-    oracle.fwd_bwd(h, W, x.idx[:rows], x.logit[:rows], m, x.T)
+    if grads:
+        oracle.fwd_bwd(h, W, x.idx[:rows], x.logit[:rows], m, x.T)
+    else:
+        oracle.fwd(h, W, x.idx[:rows], x.logit[:rows], m, x.T)
     dt = time.perf_counter() - t0
     return dt, cores
 
@@ -481,7 +486,7 @@ def run_full_teacher(args):
 
 def run_mem_scaling(args):
     """Device memory of one fused fwd+bwd at the 201,088-vocabulary shapes for
-    N = 8K, 32K and 128K tokens at a fixed 8192-token chunk.  Extra memory (the
+    N = 8K, 32K, 128K and 256K tokens at a fixed 8192-token chunk.  Extra memory (the
     workspace) must grow as O(chunk V + N K), not O(N V).  Values of the inputs
     do not matter here, so they are drawn on the device."""
     import torch
@@ -492,7 +497,7 @@ def run_mem_scaling(args):
     g = torch.Generator(device=dev).manual_seed(0)
     W = (torch.randn(V, d, device=dev, generator=g) * 0.02).to(torch.bfloat16)
     out = []
-    for N in (8192, 32768, 131072):
+    for N in (8192, 32768, 131072, 262144):
         h = torch.randn(N, d, device=dev, generator=g).to(torch.bfloat16)
         idx = torch.randint(0, V, (N, K), device=dev, generator=g, dtype=torch.int32)
         lg = torch.randn(N, K, device=dev, generator=g)
@@ -515,6 +520,107 @@ def run_mem_scaling(args):
     print(json.dumps({"mem_scaling": out, "d": d, "V": V, "K": K}), flush=True)
 
 
+def _torch_kl_sum(h, W, idx, lg, T):
+    """Sum over rows of KL(p || q) in plain PyTorch: q the softmax of the
+    student logits h W^T / T over the whole vocabulary, p the teacher's top-K
+    logits renormalised; the N x V logit grid is built and kept for autograd."""
+    import torch
+    logq = torch.log_softmax((h @ W.t()).float() / T, dim=-1)
+    logp = torch.log_softmax(lg / T, dim=-1)
+    return (logp.exp() * (logp - logq.gather(1, idx.long()))).sum()
+
+
+def run_dense_context(args):
+    """Context for the pages' peak-memory comparison (dense KL, forward-chunked
+    KL, fused chunked KL): peak device memory and time of one fwd+bwd of the
+    distillation loss at the 201,088-vocabulary shapes for N = 8K, 32K, 64K and
+    128K tokens.  The dense and forward-chunked arms are plain PyTorch (bf16 matmul,
+    fp32 log-softmax, autograd; the forward-chunked arm loops over 8192-token
+    chunks in the forward and runs one backward); the fused arm is this
+    library's kd_topk_kl_fwd_bwd.  An arm that runs out of device memory is
+    recorded as such.  Values of the inputs do not matter for memory, so they
+    are drawn on the device."""
+    import torch
+    import top_kl_loss_token_b300 as kd
+    kd.load_library()
+    dev = torch.device("cuda", 0)
+    d, V, K, T, chunk = 2880, 201088, 100, 1.0, args.chunk or 8192
+    g = torch.Generator(device=dev).manual_seed(0)
+    W0 = (torch.randn(V, d, device=dev, generator=g) * 0.02).to(torch.bfloat16)
+    reps = max(1, min(args.steps, 3))
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize(dev)
+        ts = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize(dev)
+            ts.append(a.elapsed_time(b))
+        return float(np.median(ts))
+
+    rows = []
+    for N in (8192, 32768, 65536, 131072):
+        h0 = torch.randn(N, d, device=dev, generator=g).to(torch.bfloat16)
+        idx = torch.randint(0, V, (N, K), device=dev, generator=g, dtype=torch.int32)
+        lg = torch.randn(N, K, device=dev, generator=g) * 2.0
+        for arm in ("dense", "forward_chunked", "fused_chunked"):
+            torch.cuda.synchronize(dev)
+            torch.cuda.empty_cache()
+            base = torch.cuda.memory_allocated(dev)
+            torch.cuda.reset_peak_memory_stats(dev)
+            rec = {"N": N, "arm": arm}
+            try:
+                if arm == "fused_chunked":
+                    loss = torch.empty(1, device=dev)
+                    gh = torch.empty(N, d, device=dev)
+                    gW = torch.empty(V, d, device=dev)
+                    ws = kd.allocate_workspace(N, d, V, K, chunk, kd.KD_BF16, dev)
+
+                    def fn():
+                        kd.fwd_bwd(h0, W0, idx, lg, None, T, chunk, loss=loss, grad_h=gh,
+                                   grad_W=gW, workspace=ws)
+                    rec["grad_dtype"] = "fp32"
+                else:
+                    h = h0.detach().requires_grad_(True)
+                    W = W0.detach().requires_grad_(True)
+                    out = {}
+
+                    def fn():
+                        h.grad = None
+                        W.grad = None
+                        if arm == "dense":
+                            tot = _torch_kl_sum(h, W, idx, lg, T)
+                        else:
+                            tot = sum(_torch_kl_sum(h[r:r + chunk], W, idx[r:r + chunk],
+                                                    lg[r:r + chunk], T)
+                                      for r in range(0, N, chunk))
+                        loss_t = tot / N
+                        loss_t.backward()
+                        out["loss"] = loss_t.detach()
+                    rec["grad_dtype"] = "bf16"
+                rec["ms"] = timed(fn)
+                torch.cuda.synchronize(dev)
+                rec["peak_gib"] = torch.cuda.max_memory_allocated(dev) / 2 ** 30
+                rec["peak_over_inputs_gib"] = (torch.cuda.max_memory_allocated(dev) - base) / 2 ** 30
+                rec["loss"] = float((loss if arm == "fused_chunked" else out["loss"]).item())
+            except torch.cuda.OutOfMemoryError:
+                rec["outcome"] = "out of device memory"
+            rec["inputs_gib"] = base / 2 ** 30
+            rows.append(rec)
+            loss = gh = gW = ws = h = W = out = fn = None  # release this arm's buffers
+            torch.cuda.synchronize(dev)
+            torch.cuda.empty_cache()
+        del h0, idx, lg
+        torch.cuda.empty_cache()
+    print(json.dumps({"dense_context": rows, "d": d, "V": V, "K": K, "T": T, "chunk": chunk,
+                      "device_gib": torch.cuda.get_device_properties(dev).total_memory / 2 ** 30}),
+          flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -530,6 +636,8 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=64,
                     help="tokens per step of the reference (oracle) arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fwd", action="store_true",
+                    help="time the loss alone (kd_topk_kl_fwd: no gradients) on the same workload")
     ap.add_argument("--builder", action="store_true",
                     help="time the teacher top-K cache builder on the workload's teacher-side "
                          "shapes instead of the loss")
@@ -537,7 +645,11 @@ def main():
                     help="time the full-vocabulary loss with the teacher computed in the same "
                          "pass (teacher hidden size = the student's) instead of the top-K loss")
     ap.add_argument("--mem-scaling", action="store_true",
-                    help="report device memory at N = 8K, 32K, 128K tokens (fixed chunk) and exit")
+                    help="report device memory at N = 8K, 32K, 128K, 256K tokens (fixed chunk) "
+                         "and exit")
+    ap.add_argument("--dense-context", action="store_true",
+                    help="peak memory and time of plain-PyTorch dense and forward-chunked KL "
+                         "against the fused call at N = 8K, 32K, 64K, 128K tokens, and exit")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -560,6 +672,9 @@ def main():
 
     if args.mem_scaling:
         run_mem_scaling(args)
+        return
+    if args.dense_context:
+        run_dense_context(args)
         return
     if args.builder:
         run_builder(args)
@@ -611,6 +726,10 @@ def main():
     stream = torch.cuda.current_stream(dev)
 
     def step():
+        if args.fwd:
+            kd.fwd(h, W, idx, lg, mask, x.T, chunk, loss=loss, workspace=ws, err_flags=err,
+                   stream=stream)
+            return
         kd.fwd_bwd(h, W, idx, lg, mask, x.T, chunk, loss=loss, grad_h=grad_h, grad_W=grad_W,
                    workspace=ws, err_flags=err, stream=stream)
 
@@ -644,7 +763,8 @@ def main():
     ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
     tokens_total = N * args.steps * world
     value = tokens_total / (ms / 1000.0)
-    flops_step = 6.0 * N * d * V
+    flops_per_token = (2.0 if args.fwd else 6.0) * d * V  # logits (+ grad_h, grad_W)
+    flops_step = flops_per_token * N
     tflops = flops_step * args.steps * world / (ms / 1000.0) / 1e12 / world  # per GPU
 
     # ---------------- end to end: H2D of the step's inputs, D2H of the loss
@@ -711,12 +831,14 @@ def main():
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         rows = min(args.cpu_rows, N)
-        dtc, cores = cpu_oracle_time(x, rows)
+        dtc, cores = cpu_oracle_time(x, rows, grads=not args.fwd)
+        what = "fwd" if args.fwd else "fwd+bwd"
         cpu = {"value": rows / dtc, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-               "sample": f"fp64 oracle fwd+bwd of the first {rows} of {N} tokens ({dtc:.1f} s)"}
+               "sample": f"fp64 oracle {what} of the first {rows} of {N} tokens ({dtc:.1f} s)"}
 
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "metric": FWD_METRIC if args.fwd else METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": x.dtype,
         "data": "synthetic",
@@ -727,7 +849,7 @@ def main():
         "pct_of_bf16_peak": {"burst": tflops / peaks["bf16_tflops"],
                              "sustained": tflops / peaks["bf16_tflops_sustained"],
                              "source": peaks_src},
-        "tflops_valid_tokens_per_gpu": 6.0 * valid_tokens * d * V * args.steps / (ms / 1000.0) / 1e12,
+        "tflops_valid_tokens_per_gpu": flops_per_token * valid_tokens * args.steps / (ms / 1000.0) / 1e12,
         "hbm_kernels": hbm,
         "peak_extra_gib": peak_extra,
         "workspace_gib": ws_bytes / 2 ** 30,

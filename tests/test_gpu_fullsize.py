@@ -97,3 +97,15 @@ def test_full_size_chunk_invariance_and_token_split(kd):
     assert max_rel_err(comb, a["grad_W"]) <= 4 * 2.0 ** -9
     lcomb = (g1["loss"] * g1["n_valid"] + g2["loss"] * g2["n_valid"]) / N
     assert lcomb == pytest.approx(a["loss"], rel=1e-5)
+
+
+def test_full_size_forward_only_matches_fwd_bwd(kd):
+    # kd_topk_kl_fwd runs the same teacher preparation, pass 1 and logsumexp
+    # kernels without the gradient part: the loss must be the same number
+    x = synth.make_config(3)
+    t = to_device(x)
+    a = run_gpu(kd, x, tensors=t)
+    b = run_gpu(kd, x, tensors=t, want_grads=False)
+    assert a["err"] == 0 and b["err"] == 0
+    assert b["loss"] == pytest.approx(a["loss"], rel=1e-6)
+    np.testing.assert_array_equal(b["lse"], a["lse"])
