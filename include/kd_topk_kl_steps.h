@@ -26,11 +26,32 @@ extern "C" {
  * Where a call with these sizes keeps its intermediates inside the workspace
  * (byte offsets from the workspace base, each 256-byte aligned).  Valid after
  * a kd_topk_kl_fwd_bwd / kd_topk_kl_fwd call has completed on its stream:
- *   ctrl:      uint32 error flags at +0, int32 N_valid at +4, double loss sum at +8
- *   rows:      int32 [N]  original row of the i-th valid row (i < N_valid)
- *   lse:       fp32  [N]  lse_i of the i-th valid row (natural log, of s = z/T)
- *   loss_rows: fp32  [N]  loss term of the i-th valid row (before the 1/N_valid)
- * The other regions are scratch space whose contents are not specified.
+ *   ctrl:       uint32 error flags at +0, int32 N_valid at +4, double loss sum at +8
+ *   rows:       int32 [N]  original row of the i-th valid row (i < N_valid)
+ *   lse:        fp32  [N]  lse_i of the i-th valid row (natural log, of s = z/T)
+ *   loss_rows:  fp32  [N]  loss term of the i-th valid row (before the 1/N_valid)
+ * Teacher preparation, for every valid original row r:
+ *   idx_sorted: int32 [N, K]  row r's in-range teacher indices in increasing
+ *                             order (equal indices in any order), then
+ *                             0x7fffffff up to K entries
+ *   p_sorted:   fp32  [N, K]  the teacher probability of each of those entries
+ *                             (softmax of logit / T over the row's in-range
+ *                             entries), 0 for the padding
+ *   plogp:      fp32  [N]     sum of p ln p over row r's entries
+ *   psum:       fp32  [N]     sum of p over row r's entries (1 up to rounding)
+ * The last chunk that holds valid rows, j = (N_valid - 1) / chunk, with
+ * count = N_valid - j * chunk rows; its i-th row (i < count) is the original
+ * row rows[j * chunk + i]:
+ *   boff:       uint16 [n_pb + 1, chunk_pad]  boff[b][i] = position in that
+ *                             row's sorted entries of the first one whose
+ *                             index is >= 128 b
+ *   g:          [chunk_pad, ld_g], bf16 (KD_BF16) or fp32 (KD_FP32), after
+ *               kd_topk_kl_fwd_bwd only: the gradient of the loss with respect
+ *               to the student logits, row i column v < V holding
+ *               (softmax(s_i)_v - sum of p over the row's entries with index v)
+ *               / (T N_valid) rounded to the type, columns V .. ld_g - 1 zero
+ * The other regions, and the rows of boff and g beyond count, are scratch
+ * space whose contents are not specified.
  */
 typedef struct {
   int64_t chunk;      /* resolved chunk, in tokens                              */

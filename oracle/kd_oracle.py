@@ -154,6 +154,37 @@ def fwd(h, W, topk_idx, topk_logit, mask, T, block_rows=256):
     return fwd_bwd(h, W, topk_idx, topk_logit, mask, T, block_rows, want_grads=False)
 
 
+def teacher_plogp(p):
+    """Per-row sum_k p_k ln p_k of teacher probabilities p [N,K] (0 ln 0 = 0):
+    the teacher-entropy term of loss_r."""
+    return _plogp(_f64(p))
+
+
+def grad_logits(h, W, topk_idx, topk_logit, mask, T, block_rows=256):
+    """The dense gradient of the loss with respect to the student logits,
+    dL/dz [N,V] in float64 (zero rows for rows that are not valid), computed
+    block by block exactly as inside fwd_bwd.  grad_h = (dL/dz) W and
+    grad_W = (dL/dz)^T h.  Returns a dict with G, lse, p, valid, n_valid."""
+    H = _f64(h)
+    Wd = _f64(W)
+    N = H.shape[0]
+    V = Wd.shape[0]
+    p, valid, _ = teacher_distribution(topk_idx, topk_logit, mask, V, T)
+    n_valid = int(valid.sum())
+    idx = np.asarray(topk_idx, dtype=np.int64)
+    G = np.zeros((N, V))
+    lse = np.full(N, np.nan)
+    for r0 in range(0, N, block_rows):
+        r1 = min(N, r0 + block_rows)
+        v = valid[r0:r1]
+        if not v.any():
+            continue
+        l_b, _, G_b = _row_block(H[r0:r1], Wd, idx[r0:r1], p[r0:r1], v, T, n_valid)
+        lse[r0:r1] = np.where(v, l_b, np.nan)
+        G[r0:r1] = G_b
+    return dict(G=G, lse=lse, p=p, valid=valid, n_valid=n_valid)
+
+
 def sampled_rows(h, W, topk_idx, topk_logit, mask, T, rows, block_rows=64):
     """Per-row results for a subset of rows, each computed on its own.
 

@@ -46,6 +46,8 @@ def run_gpu(kd, x, chunk=0, want_grads=True, tensors=None):
         rows=kd.workspace_view(ws, lay, "rows", N, torch.int32)[:n_valid].cpu().numpy(),
         lse=kd.workspace_view(ws, lay, "lse", N, torch.float32)[:n_valid].cpu().numpy(),
         loss_rows=kd.workspace_view(ws, lay, "loss_rows", N, torch.float32)[:n_valid].cpu().numpy(),
+        ws=ws,
+        lay=lay,
     )
     return out
 

@@ -91,9 +91,10 @@ def test_full_size_chunk_invariance_and_token_split(kd):
     comb = (g1["grad_W"] * g1["n_valid"] + g2["grad_W"] * g2["n_valid"]) / N
     # Unlike the chunk change above, the split changes N_valid, so each run
     # scales its bf16 gradient tile by a different 1/(T N_valid) and rounds it
-    # on its own: the stored exponentials (rel. 2^-9 on q) and the tile itself
-    # (rel. 2^-9 on G) carry up to 2^-9 (|q| + |G|) each, so two runs may
-    # differ by about 4 * 2^-9 = 7.8e-3 of the largest entry.
+    # on its own: the stored exponentials (rel. up to 2^-8 on q, bf16 has an
+    # 8-bit significand) and the tile itself (up to 2^-8 on G) carry up to
+    # 2^-8 (|q| + |G|), and the two runs' roundings are independent: allow
+    # 2^-7 = 7.8e-3 of the largest entry.
     assert max_rel_err(comb, a["grad_W"]) <= 4 * 2.0 ** -9
     lcomb = (g1["loss"] * g1["n_valid"] + g2["loss"] * g2["n_valid"]) / N
     assert lcomb == pytest.approx(a["loss"], rel=1e-5)

@@ -156,8 +156,8 @@ def test_zero_loss_when_teacher_equals_student(kd):
     x = synth.KDInputs("eq", "bf16", synth.bf16_bits(hv), synth.bf16_bits(np.eye(V, dtype=np.float32)),
                        idx, np.take_along_axis(hv, idx, axis=1).astype(np.float32), None, 1.0, 0)
     got = run_gpu(kd, x)
-    # The stored exponentials are bf16 (relative error 2^-9), so the gradient
-    # is zero up to about 2^-9 of a typical entry 1 / (T N) = 0.004.
+    # The stored exponentials are bf16 (relative error up to 2^-8), so the
+    # gradient is zero up to about 2^-8 of a typical entry 1 / (T N) = 0.004.
     assert abs(got["loss"]) < 1e-4
     assert np.abs(got["grad_h"]).max() < 2e-5 and np.abs(got["grad_W"]).max() < 2e-5
 

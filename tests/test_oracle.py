@@ -164,6 +164,36 @@ def test_autograd_matches(T):
     np.testing.assert_allclose(r["grad_W"], tW.grad.numpy(), rtol=1e-10, atol=1e-15)
 
 
+@pytest.mark.parametrize("distinct", [True, False])
+def test_grad_logits_is_autograd_in_the_logits(distinct):
+    # dL/dz from autograd of the loss written on z directly (a duplicate index
+    # is gathered twice, so autograd adds both probabilities)
+    h, W, idx, logit, _ = rand_problem(N=10, d=6, V=21, K=5, seed=31, distinct=distinct)
+    mask = np.array([1, 0, 1, 1, 1, 1, 0, 1, 1, 1], np.uint8)
+    T = 1.7
+    z = torch.tensor(h @ W.T, requires_grad=True)
+    logq = torch.log_softmax(z / T, dim=1)
+    p = torch.softmax(torch.tensor(logit) / T, dim=1)
+    lq = torch.gather(logq, 1, torch.tensor(idx, dtype=torch.int64))
+    per_row = (p * (torch.log(p) - lq)).sum(dim=1)
+    m = torch.tensor(mask != 0)
+    (per_row[m].sum() / m.sum()).backward()
+    g = oracle.grad_logits(h, W, idx, logit, mask, T, block_rows=3)
+    np.testing.assert_allclose(g["G"], z.grad.numpy(), rtol=1e-10, atol=1e-16)
+    assert g["n_valid"] == 8 and np.all(g["G"][mask == 0] == 0)
+    # and it is the factor the weight gradients are built from
+    r = oracle.fwd_bwd(h, W, idx, logit, mask, T)
+    np.testing.assert_allclose(g["G"] @ W, r["grad_h"], rtol=1e-12, atol=1e-16)
+    np.testing.assert_allclose(g["lse"][mask != 0], r["lse"][mask != 0], rtol=1e-14)
+
+
+def test_teacher_plogp_closed_forms():
+    K = 6
+    p = np.array([[1.0 / K] * K, [1.0, 0, 0, 0, 0, 0], [0.5, 0.5, 0, 0, 0, 0]])
+    np.testing.assert_allclose(oracle.teacher_plogp(p), [-math.log(K), 0.0, -math.log(2.0)],
+                               rtol=1e-15, atol=1e-16)
+
+
 # ------------------------------------------------------------ finite differences
 
 @pytest.mark.parametrize("distinct", [True, False])

@@ -410,8 +410,9 @@ def status_string(st: int) -> str:
 
 
 def workspace_view(workspace, lay: WorkspaceLayout, name: str, count: int, dtype):
-    """A typed view of one documented region of a workspace (see
-    kd_topk_kl_workspace_layout): 'ctrl', 'rows', 'lse' or 'loss_rows'."""
+    """A typed view of the first `count` elements of one documented region of a
+    workspace (see kd_topk_kl_workspace_layout), e.g. 'rows', 'lse',
+    'idx_sorted', 'p_sorted', 'plogp', 'boff' or 'g'."""
     import torch
     off = getattr(lay, "off_" + name)
     nbytes = count * torch.empty(0, dtype=dtype).element_size()
