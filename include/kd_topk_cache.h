@@ -42,9 +42,10 @@ extern "C" {
  * Bytes of device workspace for a call with these sizes (chunk <= 0: the
  * default chunk).  Returns 0 for invalid sizes.  Per chunk of positions it
  * holds each row's largest key per 128-column vocabulary block
- * (8 * ceil(V / 128) bytes per row) and the row's candidate list, which is
- * bounded by 128 K entries (8 bytes each): the candidates all lie in the K
- * blocks whose largest key reaches the row's K-th largest block key.
+ * (8 * ceil(V / 128) bytes per row), the row's threshold, count and redo mark
+ * (16 bytes) and its candidate list of up to 128 K entries (8 bytes each):
+ * with the row's K-th largest block key as threshold the candidates all lie
+ * in the K blocks whose largest key reaches it.
  */
 size_t kd_topk_cache_workspace_bytes(int64_t N, int64_t d, int64_t V, int32_t K, int64_t chunk);
 
@@ -53,10 +54,15 @@ int64_t kd_topk_cache_default_chunk(int64_t N, int64_t V, int32_t K);
 
 /*
  * Writes the top-K cache of h against W.  Per chunk of positions: a
- * tensor-core pass computes z tile by tile and keeps each 128-column block's
- * largest rank key; each row's threshold is its K-th largest block key; a
- * second pass recomputes the same tiles (bit-identical) and collects every
- * key that reaches the threshold; a final selection sorts the row's K best.
+ * tensor-core pass computes z for the first max(K, V / 1024) blocks of 128
+ * columns only and keeps each block's largest rank key; each row's threshold
+ * is the K-th largest of those keys (at least K logits reach it, so no top-K
+ * logit is below it); a second pass computes all of z with the same tiles
+ * (bit-identical logits), keeps every block's largest key and collects every
+ * key that reaches the threshold; a selection sorts each row's K best.  A row
+ * whose candidates outgrow 128 K takes the K-th largest of all its block keys
+ * as threshold instead and is collected again by a third pass, which does no
+ * work when no row overflowed.
  * Errors: KD_ERR_INVALID_ARG (a NULL pointer, N < 0, d, V or K < 1, K > V),
  * KD_ERR_UNSUPPORTED (d % 8 != 0, K > KD_MAX_K, sizes beyond 2^31),
  * KD_ERR_WORKSPACE, KD_ERR_CUDA.  With N = 0 nothing is launched.

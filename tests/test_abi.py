@@ -125,7 +125,7 @@ def test_topk_cache_argument_errors_and_plan(lib):
     assert call(h=264) == 1              # misaligned
     # candidates are bounded by 128 K per row, block keys by V / 128 per row
     n = kd.topk_cache_workspace_bytes(8192, 2880, 201088, 100, 8192)
-    per_row = 8 * (128 * 100 + 1571 + 1) + 4
+    per_row = 8 * (128 * 100 + 1571 + 1) + 8
     assert 8192 * per_row <= n <= 8192 * per_row + 4096
     assert lib.kd_topk_cache_default_chunk(32768, 201088, 100) % 128 == 0
 

@@ -73,6 +73,32 @@ def test_constant_rows_fill_the_candidate_bound(kd):
     np.testing.assert_array_equal(gv, ov.astype(np.float32))
 
 
+@pytest.mark.parametrize("chunk", [0, 128])
+def test_sampled_threshold_overflow_is_redone_exactly(kd, chunk):
+    # V = 8192 is 64 blocks and K = 4, so the first threshold comes from the
+    # first 8 blocks (1024 columns), where every logit is 0.  Rows with
+    # h = 1 have logits >= 16 in all 7168 later columns: far more candidates
+    # than the capacity of 128 K = 512, so they are redone with the tight
+    # threshold.  Rows with h = -1 keep the sampled threshold (385
+    # candidates), random rows fall either way; with 128-row chunks the
+    # second chunk (all h = -1) has no overflowing row, so its third pass
+    # returns at once.
+    rng = np.random.default_rng(21)
+    d, V, N, K = 16, 8192, 250, 4
+    W = np.zeros((V, d), np.float32)
+    W[1024:] = rng.integers(1, 4, size=(V - 1024, d))
+    h = rng.integers(-2, 3, size=(N, d)).astype(np.float32)
+    h[:40] = 1.0
+    h[40:80] = -1.0
+    h[128:] = -1.0
+    gi, gv, err = _run(kd, h, W, K, chunk)
+    oi, ov = oracle.topk_cache(h, W, K)
+    assert err == 0
+    np.testing.assert_array_equal(gi, oi)
+    np.testing.assert_array_equal(gv, ov.astype(np.float32))
+    np.testing.assert_array_equal(gi[50], np.arange(K))
+
+
 def test_nan_hidden_state_ranks_last_and_is_flagged(kd):
     h, W = _int_inputs(9, 64, 32, 1000)
     h[5, 3] = np.nan

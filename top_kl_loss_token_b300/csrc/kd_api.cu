@@ -44,7 +44,7 @@ const char* const kKindNames[kNumKinds] = {
     "pass1_gemm",   "lse_combine", "grad_tile",        "bwd_gemm",    "finalize",
     "simt_pass1",   "simt_gemm",   "topk_block_max",   "topk_threshold",
     "topk_candidates", "topk_select", "mask_rows", "full_pass1_gemm", "full_lse_combine",
-    "full_grad_tile"};
+    "full_grad_tile", "topk_refine", "topk_redo"};
 
 struct TimingRec {
   int kind;

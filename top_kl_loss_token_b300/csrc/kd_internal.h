@@ -75,6 +75,8 @@ enum KernelKind {
   kFullPass1Gemm,
   kFullLseCombine,
   kFullGradTile,
+  kTopkRefine,
+  kTopkRedo,
   kNumKinds
 };
 
@@ -274,6 +276,8 @@ struct TopkGemmArgs {
   const void* h;      // [count, d] bf16, the chunk's first row
   const void* W;      // [V, d] bf16
   int64_t count, d, V;
+  int64_t v_cols;     // logits computed: vocabulary columns [0, v_cols)
+  const uint32_t* gate;  // optional: the launch does nothing while *gate == 0
   uint64_t* bkey;     // [count][ceil(V / 128)]
   const uint64_t* tau;
   uint32_t* cnt;

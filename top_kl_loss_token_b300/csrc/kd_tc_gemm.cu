@@ -133,6 +133,7 @@ struct KParams {
   uint32_t* err;
   uint64_t wait_limit_ns;  // 0: the default limit
   int withhold_arrival;    // test of the bounded waits: never announce stage 0's bytes
+  const uint32_t* gate;    // when set and *gate == 0, the launch has no work
   // pass-1 epilogue
   float k2;
   int V;
@@ -149,8 +150,9 @@ struct KParams {
   uint16_t* u;
   int64_t ldg;
   // top-K cache epilogues (rows are the chunk's positions, columns the vocabulary)
-  uint64_t* bkey;        // [count][n_pb] largest rank key of each 128-column block
-  const uint64_t* tau;   // [count] rank key of the K-th largest block key
+  uint64_t* bkey;        // [count][bkey_ld] largest rank key of each 128-column block
+  int64_t bkey_ld;
+  const uint64_t* tau;   // [count] the row's candidate threshold
   uint32_t* cnt;         // [count] candidates appended so far
   uint64_t* cand;        // [count][cap] candidate rank keys
   int64_t cap;
@@ -177,6 +179,7 @@ __device__ __forceinline__ Sizes get_sizes(const KParams& P) {
   }
   s.count = count;
   s.total = 0;
+  if (P.gate != nullptr && *P.gate == 0u) return s;
 #pragma unroll
   for (int pi = 0; pi < 2; ++pi) {
     int M = P.M[pi], N = P.N[pi], K = P.K[pi];
@@ -699,27 +702,31 @@ __device__ __forceinline__ uint64_t max_key32(const float (&v)[N], int col, int 
   return best;
 }
 
-__device__ __forceinline__ void append_ge(const float (&v)[32], int col, int nvalid, uint64_t tau,
-                                          uint32_t* cnt, uint64_t* cand, int64_t cap,
-                                          uint32_t* err) {
+// The block maximum as in max_key32, and every key >= tau appended to the
+// row's candidate list (slots past the capacity are counted, not written).
+__device__ __forceinline__ uint64_t max_append32(const float (&v)[32], int col, int nvalid,
+                                                 uint64_t best, uint64_t tau, uint32_t* cnt,
+                                                 uint64_t* cand, int64_t cap) {
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
     if (j < nvalid) {
       const uint64_t k = rank_key(v[j], static_cast<uint32_t>(col + j));
+      best = k > best ? k : best;
       if (k >= tau) {
         const uint32_t slot = atomicAdd(cnt, 1u);
         if (slot < cap) cand[slot] = k;
-        else atomicOr(err, KD_FLAG_INTERNAL);
       }
     }
   }
+  return best;
 }
 
 // Top-K cache epilogues.  Each thread owns one row and one 128-column block
 // of the tile.
 //   kModeTopkMax:  the block's largest rank key -> bkey[row][block];
-//   kModeTopkCand: if the block's largest key reaches the row's threshold
-//                  tau, append every key >= tau to the row's candidates.
+//   kModeTopkCand: the same, and every key >= the row's threshold tau is
+//                  appended to the row's candidates (the count goes on past
+//                  the capacity, so an overflowing row is recognisable).
 template <int MODE>
 __device__ void epilogue_topk(const KParams& P, const Sizes& S, Ctl* ctl, uint32_t tmem,
                               const WaitCtx& wc, int warp, int lane, int rank) {
@@ -748,12 +755,8 @@ __device__ void epilogue_topk(const KParams& P, const Sizes& S, Ctl* ctl, uint32
     const int col0 = tl.n * kBN + half * 128;
     const int pb = tl.n * 2 + half;
     const bool live = (i < S.count) && (pb < P.n_pb);
-    bool scan = live;
     uint64_t tau = 0;
-    if (MODE == kModeTopkCand && live) {
-      tau = P.tau[i];
-      scan = P.bkey[static_cast<int64_t>(i) * P.n_pb + pb] >= tau;
-    }
+    if (MODE == kModeTopkCand && live) tau = P.tau[i];
     ok = mbar_wait(&ctl->tfull[b], tp, wc);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) break;
@@ -765,23 +768,23 @@ __device__ void epilogue_topk(const KParams& P, const Sizes& S, Ctl* ctl, uint32
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->tempty[b]), 0));
-    if (!scan) continue;
+    if (!live) continue;
     const int nv = min(128, P.V - col0);
+    uint64_t best = 0;
     if (MODE == kModeTopkMax) {
-      uint64_t best = 0;
       best = max_key32(v0, col0, nv, best);
       best = max_key32(v1, col0 + 32, nv - 32, best);
       best = max_key32(v2, col0 + 64, nv - 64, best);
       best = max_key32(v3, col0 + 96, nv - 96, best);
-      P.bkey[static_cast<int64_t>(i) * P.n_pb + pb] = best;
     } else {
       uint32_t* cnt = P.cnt + i;
       uint64_t* cand = P.cand + static_cast<int64_t>(i) * P.cap;
-      append_ge(v0, col0, nv, tau, cnt, cand, P.cap, P.err);
-      append_ge(v1, col0 + 32, nv - 32, tau, cnt, cand, P.cap, P.err);
-      append_ge(v2, col0 + 64, nv - 64, tau, cnt, cand, P.cap, P.err);
-      append_ge(v3, col0 + 96, nv - 96, tau, cnt, cand, P.cap, P.err);
+      best = max_append32(v0, col0, nv, best, tau, cnt, cand, P.cap);
+      best = max_append32(v1, col0 + 32, nv - 32, best, tau, cnt, cand, P.cap);
+      best = max_append32(v2, col0 + 64, nv - 64, best, tau, cnt, cand, P.cap);
+      best = max_append32(v3, col0 + 96, nv - 96, best, tau, cnt, cand, P.cap);
     }
+    P.bkey[static_cast<int64_t>(i) * P.bkey_ld + pb] = best;
   }
 }
 
@@ -1216,7 +1219,7 @@ cudaError_t launch_tc_topk(const TopkGemmArgs& g, int pass, cudaStream_t s) {
   P.tmB[1] = P.tmB[0];
   P.a_load[0] = P.b_load[0] = kLoadK;
   P.M[0] = static_cast<int>(g.count);
-  P.N[0] = static_cast<int>(g.V);
+  P.N[0] = static_cast<int>(g.v_cols);
   P.K[0] = static_cast<int>(g.d);
   P.bn[0] = kBN;  // the epilogue's 128-column blocks need full 256-wide tiles
   P.tx_bytes[0] = 2u * kStageBytes;
@@ -1224,9 +1227,11 @@ cudaError_t launch_tc_topk(const TopkGemmArgs& g, int pass, cudaStream_t s) {
   P.chunk = static_cast<int>(g.count);
   P.counter = g.counter;
   P.err = g.err;
-  P.V = static_cast<int>(g.V);
-  P.n_pb = static_cast<int>(ceil_div(g.V, kPB));
+  P.V = static_cast<int>(g.v_cols);
+  P.n_pb = static_cast<int>(ceil_div(g.v_cols, kPB));
   P.bkey = g.bkey;
+  P.bkey_ld = ceil_div(g.V, kPB);
+  P.gate = g.gate;
   P.tau = g.tau;
   P.cnt = g.cnt;
   P.cand = g.cand;

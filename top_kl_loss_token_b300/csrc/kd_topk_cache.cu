@@ -11,12 +11,26 @@
 // Every logit is compared through a 64-bit rank key (kd_tc_gemm.cu,
 // rank_key): the high word orders the float, the low word makes the lower
 // vocabulary index win among equal logits, so all keys of a row are distinct.
-// Pass 1 stores each 128-column block's largest key.  The row's threshold tau
-// is its K-th largest block key: exactly K blocks reach tau, so at least K
-// logits do, and every key >= tau lies in one of those K blocks -- at most
-// 128 K candidates whatever the data (ties included).  Pass 2 recomputes the
-// same tiles (same kernel, same accumulation order: bit-identical logits) and
-// appends the keys >= tau; the selection then takes the K largest.
+//
+// A row's candidate threshold is the K-th largest of the largest keys of
+// some set of its 128-column blocks: those K block maxima are K distinct keys
+// at or above it, so the row's K-th largest key is too, and every top-K key
+// is a candidate.  Over ALL blocks the threshold is tight: exactly K blocks
+// reach it, so the candidates lie in K blocks -- at most 128 K of them
+// whatever the data (ties included).  Over a sample of blocks it may be lower
+// and let more candidates through, but the sample costs only its share of the
+// logits.  So, per chunk of positions:
+//   pass 1  the tensor cores compute the logits of the first n_s blocks only
+//           (n_s = max(K, n_pb / 8), whole 256-column tiles) and keep each
+//           block's largest key; tau = the K-th largest of them;
+//   pass 2  all logits; each block's largest key is stored and every key
+//           >= tau appended to the row's candidate list (capacity 128 K);
+//   select  the K largest candidates of every row that did not overflow;
+//   exact   rows that overflowed take the tight threshold from the block keys
+//           of pass 2, and a third, gated pass (it returns at once when no row
+//           overflowed) collects their candidates again for a second select.
+// Every pass runs the same kernel with the same 256-wide tiles and the same
+// accumulation order, so a logit is bit-identical in all of them.
 #include <string.h>
 
 #include <algorithm>
@@ -75,27 +89,62 @@ __device__ uint64_t kth_largest(const uint64_t* __restrict__ keys, int64_t n, in
   return prefix;
 }
 
-// tau[i] = the K-th largest block key of row i (0 -- below every key -- when
-// the row has fewer than K blocks, so that every logit is a candidate).
+// tau[i] = the K-th largest of the first nb block keys of row i (0 -- below
+// every key -- when nb < K, so that every logit is a candidate).
 __global__ void __launch_bounds__(kSelThreads) threshold_kernel(const uint64_t* __restrict__ bkey,
-                                                                int64_t n_pb, int64_t K,
+                                                                int64_t ld, int64_t nb, int64_t K,
                                                                 uint64_t* __restrict__ tau) {
   const int64_t i = blockIdx.x;
   uint64_t t = 0;
-  if (K <= n_pb) t = kth_largest(bkey + i * n_pb, n_pb, K);
+  if (K <= nb) t = kth_largest(bkey + i * ld, nb, K);
   if (threadIdx.x == 0) tau[i] = t;
 }
 
+// After a pass with a sampled threshold: a row whose candidates overflowed the
+// capacity gets the tight threshold over all n_pb block keys, an empty list
+// and its mark set, and opens the gate of the next pass; every other row gets
+// a threshold above every key, so that pass appends nothing for it.
+__global__ void __launch_bounds__(kSelThreads) refine_kernel(const uint64_t* __restrict__ bkey,
+                                                             int64_t n_pb, int64_t K, int64_t cap,
+                                                             uint64_t* __restrict__ tau,
+                                                             uint32_t* __restrict__ cnt,
+                                                             uint32_t* __restrict__ redo,
+                                                             uint32_t* __restrict__ gate) {
+  const int64_t i = blockIdx.x;
+  if (static_cast<int64_t>(cnt[i]) <= cap) {
+    if (threadIdx.x == 0) {
+      tau[i] = ~0ull;
+      redo[i] = 0u;
+    }
+    return;
+  }
+  const uint64_t t = kth_largest(bkey + i * n_pb, n_pb, K);
+  if (threadIdx.x == 0) {
+    tau[i] = t;
+    cnt[i] = 0u;
+    redo[i] = 1u;
+    atomicExch(gate, 1u);
+  }
+}
+
 // The K largest candidate keys of row i, sorted, decoded into (index, logit).
+//   mode 0: every row (tight thresholds: a row never overflows);
+//   mode 1: rows that did not overflow (the others are redone);
+//   mode 2: the redone rows only (redo[i] != 0; tight thresholds).
 __global__ void __launch_bounds__(kSelThreads) select_kernel(
     const uint64_t* __restrict__ cand, int64_t cap, const uint32_t* __restrict__ cnt, int K,
-    int P2, int32_t* __restrict__ out_idx, float* __restrict__ out_val,
-    uint32_t* __restrict__ err) {
+    int P2, int mode, const uint32_t* __restrict__ redo, int32_t* __restrict__ out_idx,
+    float* __restrict__ out_val, uint32_t* __restrict__ err) {
   extern __shared__ uint64_t skey[];
   __shared__ int s_n;
   const int64_t i = blockIdx.x;
   int64_t c = cnt[i];
-  if (c > cap) c = cap;  // cannot happen (the candidates are bounded by 128 K)
+  if (mode == 1 && c > cap) return;
+  if (mode == 2 && redo[i] == 0u) return;
+  if (c > cap) {  // cannot happen: a tight threshold bounds the candidates by 128 K
+    if (threadIdx.x == 0) atomicOr(err, KD_FLAG_INTERNAL);
+    c = cap;
+  }
   const uint64_t* row = cand + i * cap;
   const uint64_t kth = c >= K ? kth_largest(row, c, K) : 0;
   if (threadIdx.x == 0) s_n = 0;
@@ -139,7 +188,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
 
 struct CachePlan {
   int64_t chunk, n_pb, cap;
-  size_t off_ctrl, off_bkey, off_tau, off_cnt, off_cand, off_sched, total;
+  int64_t n_s;  // blocks whose logits set the first threshold
+  size_t off_ctrl, off_bkey, off_tau, off_cnt, off_redo, off_cand, off_sched, total;
 };
 
 bool valid_sizes(int64_t N, int64_t d, int64_t V, int32_t K) {
@@ -153,6 +203,10 @@ kd_status cache_plan(int64_t N, int64_t d, int64_t V, int32_t K, int64_t chunk, 
     return KD_ERR_UNSUPPORTED;
   p->n_pb = ceil_div(V, kPB);
   p->cap = std::min<int64_t>(int64_t(kPB) * K, p->n_pb * kPB);
+  // at least K blocks, an eighth of the vocabulary, whole 256-column tiles
+  int64_t ns = std::max<int64_t>(K, ceil_div(p->n_pb, int64_t(8)));
+  ns = round_up(ns, int64_t(kBN / kPB));
+  p->n_s = std::min(ns, p->n_pb);
   int64_t c = chunk > 0 ? chunk : kd_topk_cache_default_chunk(N, V, K);
   if (N > 0 && c > N) c = N;
   if (c < 1) c = 1;
@@ -169,6 +223,7 @@ kd_status cache_plan(int64_t N, int64_t d, int64_t V, int32_t K, int64_t chunk, 
   p->off_bkey = take(8 * cs * static_cast<size_t>(p->n_pb));
   p->off_tau = take(8 * cs);
   p->off_cnt = take(4 * cs);
+  p->off_redo = take(4 * cs);
   p->off_cand = take(8 * cs * static_cast<size_t>(p->cap));
   p->off_sched = take(256);
   p->total = o;
@@ -185,7 +240,7 @@ int64_t kd_topk_cache_default_chunk(int64_t N, int64_t V, int32_t K) {
   // About 2 GiB of per-chunk buffers; equal chunks, multiples of 128 rows.
   const int64_t n_pb = kd::ceil_div(V, kd::kPB);
   const int64_t cap = std::min<int64_t>(int64_t(kd::kPB) * K, n_pb * kd::kPB);
-  const int64_t per_row = 8 * (n_pb + cap + 1) + 4;
+  const int64_t per_row = 8 * (n_pb + cap + 1) + 8;
   int64_t cmax = (int64_t(2) << 30) / per_row;
   cmax = cmax / kd::kBM * kd::kBM;
   if (cmax < kd::kBM) cmax = kd::kBM;
@@ -222,9 +277,11 @@ kd_status kd_topk_cache_build(const void* h, const void* W, int64_t N, int64_t d
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint32_t* err = dev_err_flags != nullptr ? dev_err_flags : reinterpret_cast<uint32_t*>(ws + P.off_ctrl);
+  uint32_t* gate = reinterpret_cast<uint32_t*>(ws + P.off_ctrl + 8);
   uint64_t* bkey = reinterpret_cast<uint64_t*>(ws + P.off_bkey);
   uint64_t* tau = reinterpret_cast<uint64_t*>(ws + P.off_tau);
   uint32_t* cnt = reinterpret_cast<uint32_t*>(ws + P.off_cnt);
+  uint32_t* redo = reinterpret_cast<uint32_t*>(ws + P.off_redo);
   uint64_t* cand = reinterpret_cast<uint64_t*>(ws + P.off_cand);
   uint32_t* sched = reinterpret_cast<uint32_t*>(ws + P.off_sched);
   if (dev_err_flags == nullptr) KD_CUDA(cudaMemsetAsync(err, 0, sizeof(uint32_t), stream));
@@ -234,9 +291,15 @@ kd_status kd_topk_cache_build(const void* h, const void* W, int64_t N, int64_t d
   const size_t sel_smem = static_cast<size_t>(P2) * sizeof(uint64_t);
   KD_CUDA(cudaFuncSetAttribute(kd::select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(sel_smem)));
+  // With every block sampled the first threshold is already tight.
+  const bool sampled = P.n_s < P.n_pb;
+  const int64_t v_s = std::min<int64_t>(V, P.n_s * kd::kPB);
 
   for (int64_t row0 = 0; row0 < N; row0 += P.chunk) {
     const int64_t count = std::min<int64_t>(P.chunk, N - row0);
+    const unsigned rows = static_cast<unsigned>(count);
+    int32_t* oi = topk_idx + row0 * K;
+    float* ov = topk_logit + row0 * K;
     kd::TopkGemmArgs g;
     memset(&g, 0, sizeof(g));
     g.h = static_cast<const uint8_t*>(h) + row0 * d * 2;
@@ -244,6 +307,7 @@ kd_status kd_topk_cache_build(const void* h, const void* W, int64_t N, int64_t d
     g.count = count;
     g.d = d;
     g.V = V;
+    g.v_cols = v_s;
     g.bkey = bkey;
     g.tau = tau;
     g.cnt = cnt;
@@ -252,27 +316,26 @@ kd_status kd_topk_cache_build(const void* h, const void* W, int64_t N, int64_t d
     g.counter = sched;
     g.err = err;
     g.num_sms = sms;
-    {
-      kd::TimedLaunch tl(kd::kTopkBlockMax, stream);
-      KD_CUDA(kd::launch_tc_topk(g, 1, stream));
-    }
-    {
-      kd::TimedLaunch tl(kd::kTopkThreshold, stream);
-      kd::threshold_kernel<<<static_cast<unsigned>(count), kd::kSelThreads, 0, stream>>>(
-          bkey, P.n_pb, K, tau);
-      KD_CUDA(cudaGetLastError());
-    }
+    KD_LAUNCH(kd::kTopkBlockMax, kd::launch_tc_topk(g, 1, stream));
+    KD_LAUNCH(kd::kTopkThreshold, (kd::threshold_kernel<<<rows, kd::kSelThreads, 0, stream>>>(
+                                       bkey, P.n_pb, P.n_s, K, tau),
+                                   cudaGetLastError()));
     KD_CUDA(cudaMemsetAsync(cnt, 0, sizeof(uint32_t) * static_cast<size_t>(count), stream));
-    {
-      kd::TimedLaunch tl(kd::kTopkCandidates, stream);
-      KD_CUDA(kd::launch_tc_topk(g, 2, stream));
-    }
-    {
-      kd::TimedLaunch tl(kd::kTopkSelect, stream);
-      kd::select_kernel<<<static_cast<unsigned>(count), kd::kSelThreads, sel_smem, stream>>>(
-          cand, P.cap, cnt, K, P2, topk_idx + row0 * K, topk_logit + row0 * K, err);
-      KD_CUDA(cudaGetLastError());
-    }
+    g.v_cols = V;
+    KD_LAUNCH(kd::kTopkCandidates, kd::launch_tc_topk(g, 2, stream));
+    KD_LAUNCH(kd::kTopkSelect, (kd::select_kernel<<<rows, kd::kSelThreads, sel_smem, stream>>>(
+                                    cand, P.cap, cnt, K, P2, sampled ? 1 : 0, redo, oi, ov, err),
+                                cudaGetLastError()));
+    if (!sampled) continue;
+    KD_CUDA(cudaMemsetAsync(gate, 0, sizeof(uint32_t), stream));
+    KD_LAUNCH(kd::kTopkRefine, (kd::refine_kernel<<<rows, kd::kSelThreads, 0, stream>>>(
+                                       bkey, P.n_pb, K, P.cap, tau, cnt, redo, gate),
+                                   cudaGetLastError()));
+    g.gate = gate;
+    KD_LAUNCH(kd::kTopkRedo, kd::launch_tc_topk(g, 2, stream));
+    KD_LAUNCH(kd::kTopkRefine, (kd::select_kernel<<<rows, kd::kSelThreads, sel_smem, stream>>>(
+                                    cand, P.cap, cnt, K, P2, 2, redo, oi, ov, err),
+                                cudaGetLastError()));
   }
   return KD_OK;
 }
