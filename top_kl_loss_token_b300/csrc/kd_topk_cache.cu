@@ -55,9 +55,13 @@ __device__ __forceinline__ int32_t key_index(uint64_t k) {
   return static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(k));
 }
 
-// The k-th largest (1-based) of n distinct 64-bit keys keys[0 .. n), by
-// radix selection on 8-bit digits from the most significant one.  Called by
-// every thread of the block; returns the same key to all of them.
+// The k-th largest (1-based, 1 <= k <= n) of n distinct 64-bit keys
+// keys[0 .. n), by radix selection on 8-bit digits from the most significant
+// one.  Per digit the first warp scans the 256-bin histogram from the top:
+// lane l sums bins 255 - 8 l down to 248 - 8 l, a warp prefix sum over the
+// lanes finds the lane whose bins hold the k-th key, and that lane walks its
+// eight bins.  Called by every thread of the block (a multiple of 32
+// threads); returns the same key to all of them.
 __device__ uint64_t kth_largest(const uint64_t* __restrict__ keys, int64_t n, int64_t k) {
   __shared__ uint32_t hist[256];
   __shared__ uint64_t s_prefix;
@@ -72,15 +76,38 @@ __device__ uint64_t kth_largest(const uint64_t* __restrict__ keys, int64_t n, in
       if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-      int64_t kk = s_k;
-      int b = 255;
-      for (; b > 0; --b) {
-        if (static_cast<int64_t>(hist[b]) >= kk) break;
-        kk -= hist[b];
+    if (threadIdx.x < 32) {
+      const int lane = threadIdx.x;
+      uint32_t c[8];
+      int64_t sum = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c[j] = hist[255 - 8 * lane - j];
+        sum += c[j];
       }
-      s_k = kk;
-      s_prefix = prefix | (static_cast<uint64_t>(b) << shift);
+      int64_t incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const int64_t kk = s_k;
+      const int64_t excl = incl - sum;
+      __syncwarp();
+      if (excl < kk && kk <= incl) {
+        int64_t rem = kk - excl;
+        int b = 255 - 8 * lane;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (rem <= static_cast<int64_t>(c[j])) {
+            b = 255 - 8 * lane - j;
+            break;
+          }
+          rem -= c[j];
+        }
+        s_k = rem;
+        s_prefix = prefix | (static_cast<uint64_t>(b) << shift);
+      }
     }
     __syncthreads();
     prefix = s_prefix;
