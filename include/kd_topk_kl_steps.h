@@ -82,9 +82,11 @@ kd_status kd_topk_kl_workspace_layout(int64_t N, int64_t d, int64_t V, int32_t K
 
 /*
  * The same layout for a kd_full_kl_fwd_bwd call (kd_full_kl.h): ctrl, rows,
- * lse (of the student's s) and loss_rows as above; the regions that belong to
- * the top-K cache (sorted teacher entries, plogp, psum, part_ps, boff) do not
- * exist there and are reported as offset 0.
+ * lse (of the student's s) and loss_rows as above, and g (bf16), the last
+ * chunk's gradient with respect to the student logits, (softmax(s_i)_v -
+ * softmax(t_i)_v) / (T N_valid), in the same rows and columns as above; the
+ * regions that belong to the top-K cache (sorted teacher entries, plogp,
+ * psum, part_ps, boff) do not exist there and are reported as offset 0.
  */
 kd_status kd_full_kl_workspace_layout(int64_t N, int64_t d_s, int64_t d_t, int64_t V,
                                       int64_t chunk, kd_workspace_layout* out);

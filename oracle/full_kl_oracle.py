@@ -73,6 +73,29 @@ def full_kl_fwd_bwd(h_s, W_s, h_t, W_t, mask, T, block_rows=256, want_grads=True
                 valid=valid, n_valid=n_valid)
 
 
+def full_kl_grad_logits(h_s, W_s, h_t, W_t, mask, T):
+    """The dense gradient of the full-vocabulary loss with respect to the
+    student logits z_s = h_s W_s^T: dL/dz_s = (softmax(s) - softmax(t)) /
+    (T N_valid), zero rows for masked rows.  Returns dict(G [N, V], q (student
+    softmax), p (teacher softmax), valid, n_valid); q and p are zero on masked
+    rows."""
+    h_s = np.asarray(h_s, dtype=np.float64)
+    W_s = np.asarray(W_s, dtype=np.float64)
+    h_t = np.asarray(h_t, dtype=np.float64)
+    W_t = np.asarray(W_t, dtype=np.float64)
+    N, V = h_s.shape[0], W_s.shape[0]
+    valid = np.ones(N, dtype=bool) if mask is None else np.asarray(mask) != 0
+    n_valid = int(valid.sum())
+    q = np.zeros((N, V))
+    p = np.zeros((N, V))
+    rows = np.nonzero(valid)[0]
+    if rows.size:
+        q[rows] = np.exp(_log_softmax((h_s[rows] @ W_s.T) / T))
+        p[rows] = np.exp(_log_softmax((h_t[rows] @ W_t.T) / T))
+    G = (q - p) / (T * max(n_valid, 1))
+    return dict(G=G, q=q, p=p, valid=valid, n_valid=n_valid)
+
+
 def full_kl_sampled_rows(h_s, W_s, h_t, W_t, mask, T, rows):
     """Per-row results of the full loss for the given rows only: loss_rows,
     lse_s and grad_h rows, with N_valid over the whole batch."""

@@ -42,6 +42,23 @@ def test_kl_div_batchmean_and_its_autograd(T):
     np.testing.assert_allclose(r["grad_W"], tWs.grad.numpy(), rtol=1e-10, atol=1e-14)
 
 
+def test_grad_logits_is_autograd_of_kl_div_in_the_student_logits():
+    hs, Ws, ht, Wt = _inputs(9)
+    mask = np.ones(12, np.uint8)
+    mask[[0, 5]] = 0
+    T = 1.5
+    rows = torch.from_numpy(np.nonzero(mask)[0])
+    z = torch.tensor(hs @ Ws.T, requires_grad=True)
+    t = torch.tensor(ht @ Wt.T)
+    F.kl_div(F.log_softmax(z[rows] / T, dim=1), F.softmax(t[rows] / T, dim=1),
+             reduction="batchmean").backward()
+    g = fko.full_kl_grad_logits(hs, Ws, ht, Wt, mask, T)
+    np.testing.assert_allclose(g["G"], z.grad.numpy(), rtol=1e-10, atol=1e-16)
+    assert g["n_valid"] == 10 and np.all(g["G"][mask == 0] == 0)
+    np.testing.assert_allclose(g["q"][mask != 0].sum(axis=1), 1.0, rtol=1e-14)
+    np.testing.assert_allclose(g["p"][mask != 0].sum(axis=1), 1.0, rtol=1e-14)
+
+
 def test_zero_when_student_equals_teacher():
     hs, Ws, _, _ = _inputs(2)
     r = fko.full_kl_fwd_bwd(hs, Ws, hs, Ws, None, 1.5)

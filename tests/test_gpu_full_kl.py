@@ -48,6 +48,7 @@ def _run(kd, h_s, W_s, h_t, W_t, mask, T, chunk=0):
     nv = int(ctrl[4:8].view(np.int32)[0])
     return dict(loss=float(loss.item()), grad_h=gh.cpu().numpy().astype(np.float64),
                 grad_W=gW.cpu().numpy().astype(np.float64), err=int(err.item()), n_valid=nv,
+                ws=ws, lay=lay,
                 rows=kd.workspace_view(ws, lay, "rows", N, torch.int32)[:nv].cpu().numpy(),
                 lse=kd.workspace_view(ws, lay, "lse", N, torch.float32)[:nv].cpu().numpy(),
                 loss_rows=kd.workspace_view(ws, lay, "loss_rows", N, torch.float32)[:nv].cpu().numpy())
@@ -125,3 +126,37 @@ def test_full_vocabulary_sampled_rows(kd):
     assert max_rel_err(got["grad_h"][rows], ref["grad_h"]) <= tg
     assert got["loss"] == pytest.approx(float(np.mean(got["loss_rows"].astype(np.float64))),
                                         rel=1e-6)
+
+
+@pytest.mark.parametrize("chunk", [0, 256])
+def test_gradient_tile_and_its_products(kd, chunk):
+    # The last chunk's stored dL/dz_s against the oracle, element by element:
+    # the two stored exponentials (bf16, up to 2^-8 relative each) and the
+    # tile's own rounding stay inside 1.1 * 2^-7 (q + p) / (T N_valid).  Then
+    # grad_h rows of that chunk and (single chunk) grad_W against fp64
+    # products of the call's own tile, within 3e-5 of sum |G| |W|.
+    import torch
+    h_s, W_s, h_t, W_t, mask = _inputs(41, 600, 256, 192, 3000, w_std=0.05, mask_frac=0.2)
+    T = 2.0
+    got = _run(kd, h_s, W_s, h_t, W_t, mask, T, chunk)
+    lay = got["lay"]
+    cpad, ldg, V = int(lay.chunk_pad), int(lay.ld_g), W_s.shape[0]
+    c = min(chunk if chunk > 0 else int(lay.chunk), 600)
+    j = (got["n_valid"] - 1) // c
+    row0, count = j * c, got["n_valid"] - j * c
+    g = kd.workspace_view(got["ws"], lay, "g", cpad * ldg, torch.int16).cpu()
+    g = g.view(torch.bfloat16).double().numpy().reshape(cpad, ldg)
+    rows = got["rows"][row0:row0 + count]
+    ref = oracle.full_kl_grad_logits(h_s, W_s, h_t, W_t, mask, T)
+    scale = 1.0 / (T * ref["n_valid"])
+    G_ref = ref["G"][rows]
+    bound = 1.1 * 2.0 ** -7 * (ref["q"][rows] + ref["p"][rows]) * scale + 1e-30
+    err = np.abs(g[:count, :V] - G_ref)
+    assert np.all(err <= bound), float((err / bound).max())
+    assert np.all(g[:count, V:] == 0.0)
+    G = g[:count, :V]
+    Wd = W_s.astype(np.float64)
+    assert np.all(np.abs(got["grad_h"][rows] - G @ Wd) <= 3e-5 * (np.abs(G) @ np.abs(Wd)) + 1e-30)
+    if row0 == 0:
+        H = h_s.astype(np.float64)[rows]
+        assert np.all(np.abs(got["grad_W"] - G.T @ H) <= 3e-5 * (np.abs(G).T @ np.abs(H)) + 1e-30)

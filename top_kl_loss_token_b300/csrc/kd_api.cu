@@ -297,6 +297,7 @@ kd_status run(const void* h, const void* W, kd_dtype dtype, const int32_t* topk_
               int32_t K, float T, int64_t chunk, float* loss, float* grad_h, float* grad_W,
               bool want_grads, void* workspace, size_t ws_bytes, uint32_t* dev_err_flags,
               cudaStream_t stream) {
+  const NvtxRange range(want_grads ? "kd_topk_kl_fwd_bwd" : "kd_topk_kl_fwd");
   Plan P;
   kd_status st = make_plan(N, d, V, K, chunk, dtype, &P);
   if (st != KD_OK) return st;
@@ -330,6 +331,7 @@ kd_status run(const void* h, const void* W, kd_dtype dtype, const int32_t* topk_
   if (want_grads) KD_LAUNCH(kZeroRows, launch_zero_invalid_rows(v.row_ok, N, d, grad_h, stream));
 
   for (int64_t j = 0; j < P.n_chunks; ++j) {
+    const NvtxRange chunk_range("chunk");
     ChunkArgs a;
     a.row0 = j * P.chunk;
     a.chunk = static_cast<int>(P.chunk);

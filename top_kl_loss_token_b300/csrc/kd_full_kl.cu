@@ -125,6 +125,7 @@ kd_status kd_full_kl_fwd_bwd(const void* h_s, const void* W_s, const void* h_t, 
                              float T, int64_t chunk, float* loss, float* grad_h, float* grad_W,
                              void* workspace, size_t ws_bytes, uint32_t* dev_err_flags,
                              cudaStream_t stream) {
+  const kd::NvtxRange range("kd_full_kl_fwd_bwd");
   kd::FullPlan P;
   const kd_status st = kd::full_plan(N, d_s, d_t, V, chunk, &P);
   if (st != KD_OK) return st;
@@ -169,6 +170,7 @@ kd_status kd_full_kl_fwd_bwd(const void* h_s, const void* W_s, const void* h_t, 
   KD_LAUNCH(kd::kZeroRows, kd::launch_zero_invalid_rows(row_ok, N, d_s, grad_h, stream));
 
   for (int64_t j = 0; j < P.n_chunks; ++j) {
+    const kd::NvtxRange chunk_range("chunk");
     kd::ChunkArgs a;
     memset(&a, 0, sizeof(a));
     a.row0 = j * P.chunk;

@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include "kd_topk_kl.h"
@@ -52,6 +53,16 @@ inline int num_sms() {
     ::kd::TimedLaunch timed_launch_(kind, stream);    \
     KD_CUDA(x);                                       \
   } while (0)
+
+// A named NVTX range around a library call or one chunk of it, visible to
+// profilers that trace NVTX (ncu --nvtx); without one attached, the push and
+// pop are no-ops.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // Kernel kinds, for the optional per-launch timing (kd_timing_enable).
 enum KernelKind {

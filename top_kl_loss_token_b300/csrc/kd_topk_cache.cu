@@ -287,6 +287,7 @@ kd_status kd_topk_cache_build(const void* h, const void* W, int64_t N, int64_t d
                               int32_t K, int64_t chunk, int32_t* topk_idx, float* topk_logit,
                               void* workspace, size_t ws_bytes, uint32_t* dev_err_flags,
                               cudaStream_t stream) {
+  const kd::NvtxRange range("kd_topk_cache_build");
   kd::CachePlan P;
   const kd_status st = kd::cache_plan(N, d, V, K, chunk, &P);
   if (st != KD_OK) return st;
@@ -323,6 +324,7 @@ kd_status kd_topk_cache_build(const void* h, const void* W, int64_t N, int64_t d
   const int64_t v_s = std::min<int64_t>(V, P.n_s * kd::kPB);
 
   for (int64_t row0 = 0; row0 < N; row0 += P.chunk) {
+    const kd::NvtxRange chunk_range("chunk");
     const int64_t count = std::min<int64_t>(P.chunk, N - row0);
     const unsigned rows = static_cast<unsigned>(count);
     int32_t* oi = topk_idx + row0 * K;
