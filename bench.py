@@ -57,11 +57,17 @@ TRAFFIC_PROFILE = "profiles/dram_traffic_vocab201k-32k.md"
 
 
 def kernel_source_hash() -> str:
+    """SHA-256 of the kernel sources' code: comments removed and whitespace
+    collapsed, so that only a change of the code itself retires a capture."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for rel in TRAFFIC_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()
 
 

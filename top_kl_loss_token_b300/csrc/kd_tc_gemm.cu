@@ -17,8 +17,10 @@
 //              both in the same launch, fp32 results stored or accumulated
 //              (also the plain GEMM of kd_umma_gemm_bf16);
 //   top-K      the teacher top-K cache: the largest rank key of every
-//              128-column block (first pass), then the keys reaching each
-//              row's threshold (second pass);
+//              128-column block of a leading sample of the vocabulary (first
+//              pass), then over all of it every block's largest key and the
+//              keys reaching each row's threshold (second pass; run again,
+//              gated, for rows whose candidates overflowed);
 //   dual       the full-vocabulary loss: the teacher's and the student's
 //              logits of the same tile into the two accumulators, their block
 //              statistics and both sets of stored exponentials.
