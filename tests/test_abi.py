@@ -161,3 +161,34 @@ def test_bounded_wait_test_entry_rejects_bad_arguments(lib):
     assert f(None, 16, 16, 8, 8, 8, 1000, 16, 16, None) == 1
     assert f(16, 16, 16, 8, 8, 8, 0, 16, 16, None) == 1      # a zero time limit
     assert f(16, 16, 16, 8, 8, 12, 1000, 16, 16, None) == 2  # K % 8 != 0
+
+
+def test_product_path_fails_loudly_without_the_library(tmp_path):
+    # A copy of the package without libkd_topk_kl.so: loading the library
+    # raises, and the loss refuses host tensors before reaching it -- there is
+    # no CPU or PyTorch fallback to land on.
+    import shutil
+    import subprocess
+    import sys
+    src = os.path.join(ROOT, "top_kl_loss_token_b300")
+    shutil.copytree(src, tmp_path / "top_kl_loss_token_b300",
+                    ignore=shutil.ignore_patterns("*.so", "*.so.tmp", "__pycache__", "_build"))
+    code = (
+        "import torch\n"
+        "import top_kl_loss_token_b300 as kd\n"
+        "for f in (lambda: kd.load_library(),\n"
+        "          lambda: kd.fwd_bwd(torch.zeros(4, 8, dtype=torch.bfloat16),\n"
+        "                             torch.zeros(16, 8, dtype=torch.bfloat16),\n"
+        "                             torch.zeros(4, 2, dtype=torch.int32), torch.zeros(4, 2),\n"
+        "                             None, 1.0)):\n"
+        "    try:\n"
+        "        f()\n"
+        "        print('no error')\n"
+        "    except Exception as e:\n"
+        "        print(type(e).__name__, e)\n")
+    r = subprocess.run([sys.executable, "-c", code], cwd=tmp_path, capture_output=True, text=True,
+                       timeout=300)
+    lines = r.stdout.strip().splitlines()
+    assert len(lines) == 2, r.stdout + r.stderr
+    assert lines[0].startswith("RuntimeError") and "is missing" in lines[0], lines[0]
+    assert lines[1].startswith("ValueError") and "CUDA tensor" in lines[1], lines[1]
