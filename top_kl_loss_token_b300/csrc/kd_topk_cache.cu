@@ -5,8 +5,9 @@
 // ("Efficient Knowledge Distillation for LLMs: Offline Top-K Logits and a
 // Fused Chunked KL Loss", ai2day.live story, "What did the researchers
 // change?").  Like the loss, the cache is built without the N x V logit grid:
-// per chunk of positions the tensor cores compute z = h_c W^T twice, tile by
-// tile, and only O(chunk * (V / 128 + 128 K)) numbers are kept.
+// per chunk of positions the tensor cores compute z = h_c W^T tile by tile
+// (a leading eighth of it twice, see below), and only
+// O(chunk * (V / 128 + 128 K)) numbers are kept.
 //
 // Every logit is compared through a 64-bit rank key (kd_tc_gemm.cu,
 // rank_key): the high word orders the float, the low word makes the lower
