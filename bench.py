@@ -790,18 +790,19 @@ def main():
     torch.cuda.synchronize(dev)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e_steps):
-        h.copy_(h_pin, non_blocking=True)
-        idx.copy_(idx_pin, non_blocking=True)
-        lg.copy_(lg_pin, non_blocking=True)
-        if m_pin is not None:
-            mask.copy_(m_pin, non_blocking=True)
-        step()
-        loss_host.copy_(loss, non_blocking=True)
-        stream.synchronize()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as e_clk:
+        e0.record(stream)
+        for _ in range(e_steps):
+            h.copy_(h_pin, non_blocking=True)
+            idx.copy_(idx_pin, non_blocking=True)
+            lg.copy_(lg_pin, non_blocking=True)
+            if m_pin is not None:
+                mask.copy_(m_pin, non_blocking=True)
+            step()
+            loss_host.copy_(loss, non_blocking=True)
+            stream.synchronize()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
     barrier()
     e_value = N * e_steps * world / (max_over_ranks(e0.elapsed_time(e1), world, dev) / 1000.0)
 
@@ -869,7 +870,11 @@ def main():
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": 4},
+                "d2h_bytes_per_step": 4, "steps": e_steps,
+                # each step waits for its copies and its loss, so the GPU idles
+                # briefly between steps; under the power cap the SM clock then
+                # runs higher than in the back-to-back timed region
+                "clocks": e_clk.summary()},
         "gpu_launches": launches_total,
         "kernels": {k: {"launches": v[0], "ms": v[1]} for k, v in kernels.items()},
         "clocks": clk.summary(),
