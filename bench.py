@@ -17,6 +17,14 @@ Under torchrun (N > 1) every rank runs its own token shard of the same size
 (weak scaling, no collective on the data path); the barrier and max-over-ranks
 time use torch.distributed.  `--impl reference` times the fp64 CPU oracle on a
 bounded sample of the same workload (rank 0 only).
+
+Other modes, one JSON line each, same timing rules:
+  --fwd            the loss alone (kd_topk_kl_fwd), 2 N d V flops per step;
+  --builder        the teacher top-K cache (kd_topk_cache_build) of N positions;
+  --full-teacher   the full-vocabulary loss (kd_full_kl_fwd_bwd);
+  --mem-scaling    device memory of the fused call at N = 8K ... 256K tokens;
+  --dense-context  plain-PyTorch dense and forward-chunked KL beside the fused
+                   call: peak memory and time at N = 8K ... 128K tokens.
 """
 from __future__ import annotations
 
