@@ -554,8 +554,8 @@ def _torch_kl_sum(h, W, idx, lg, T):
 def run_dense_context(args):
     """Context for the pages' peak-memory comparison (dense KL, forward-chunked
     KL, fused chunked KL): peak device memory and time of one fwd+bwd of the
-    distillation loss at the 201,088-vocabulary shapes for N = 8K, 32K, 64K and
-    128K tokens.  The dense and forward-chunked arms are plain PyTorch (bf16 matmul,
+    distillation loss at the d, V and K of --config (default: the
+    201,088-vocabulary shapes) for N = 8K, 32K, 64K and 128K tokens.  The dense and forward-chunked arms are plain PyTorch (bf16 matmul,
     fp32 log-softmax, autograd; the forward-chunked arm loops over 8192-token
     chunks in the forward and runs one backward); the fused arm is this
     library's kd_topk_kl_fwd_bwd.  An arm that runs out of device memory is
@@ -564,8 +564,10 @@ def run_dense_context(args):
     import torch
     import top_kl_loss_token_b300 as kd
     kd.load_library()
+    from top_kl_loss_token_b300 import synth
     dev = torch.device("cuda", 0)
-    d, V, K, T, chunk = 2880, 201088, 100, 1.0, args.chunk or 8192
+    cfg = synth.CONFIGS[args.config]
+    d, V, K, T, chunk = cfg["d"], cfg["V"], cfg["K"], 1.0, args.chunk or 8192
     g = torch.Generator(device=dev).manual_seed(0)
     W0 = (torch.randn(V, d, device=dev, generator=g) * 0.02).to(torch.bfloat16)
     reps = max(1, min(args.steps, 3))
