@@ -1,8 +1,8 @@
 """Edge cases of the CUDA paths against the fp64 oracle: bitwise determinism
 of repeated calls, extreme temperatures and logit magnitudes (the online
 logsumexp must not overflow), the smallest sizes (one token, d = 8, a
-one-word vocabulary), a vocabulary smaller than one tile, and one token per
-chunk."""
+one-word vocabulary), a vocabulary smaller than one tile, one token per
+chunk, and the largest number of teacher entries (K = KD_MAX_K)."""
 import numpy as np
 import pytest
 
@@ -71,3 +71,13 @@ def test_one_token_one_word_vocabulary(kd):
 def test_small_and_ragged_sizes(kd, N, d, V, K, chunk):
     x = synth.make_inputs(N, d, V, K, T=1.0, dtype="bf16", seed=305 + N, w_std=0.2)
     _check(kd, x, chunk)
+
+
+def test_maximum_teacher_entries(kd):
+    # K = KD_MAX_K = 4096 entries per token (the teacher sort, the block
+    # offsets and the gradient tile at their largest), 150 tokens in two chunks
+    x = synth.make_inputs(150, 64, 20000, kd.KD_MAX_K, T=1.0, dtype="bf16", seed=309,
+                          mask="random0.1", w_std=0.1)
+    assert all(len(set(r.tolist())) == kd.KD_MAX_K for r in x.idx)
+    got, ref = _check(kd, x, chunk=128)
+    np.testing.assert_allclose(got["lse"], ref["lse"][got["rows"]], rtol=TOL["bf16"][0])

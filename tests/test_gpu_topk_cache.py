@@ -59,6 +59,17 @@ def test_more_entries_than_blocks_and_full_ranking(kd, K):
     np.testing.assert_array_equal(gv, ov.astype(np.float32))
 
 
+def test_maximum_k(kd):
+    # K = KD_MAX_K = 4096 of a 6000-word vocabulary (47 blocks of 128: every
+    # logit is a candidate), exact on integer inputs
+    h, W = _int_inputs(13, 130, 32, 6000)
+    gi, gv, err = _run(kd, h, W, kd.KD_MAX_K)
+    oi, ov = oracle.topk_cache(h, W, kd.KD_MAX_K)
+    assert err == 0
+    np.testing.assert_array_equal(gi, oi)
+    np.testing.assert_array_equal(gv, ov.astype(np.float32))
+
+
 def test_constant_rows_fill_the_candidate_bound(kd):
     # a zero hidden state gives equal logits everywhere: the K lowest indices,
     # and exactly 128 K candidates (the bound) in pass 2
