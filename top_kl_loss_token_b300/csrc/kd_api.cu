@@ -357,7 +357,8 @@ kd_status run(const void* h, const void* W, kd_dtype dtype, const int32_t* topk_
       p1.W = W;
       p1.d = d;
       p1.k2 = k2;
-      p1.u = static_cast<uint16_t*>(v.g);
+      // the loss alone needs no stored exponentials
+      p1.u = want_grads ? static_cast<uint16_t*>(v.g) : nullptr;
       p1.counter = v.sched;
       p1.err = err;
       p1.num_sms = sms;

@@ -206,7 +206,7 @@ struct Pass1Args {
   const void* W;   // [V, d] bf16
   int64_t d;
   float k2;        // log2(e) / T
-  uint16_t* u;     // [cpad, ldg] bf16, written
+  uint16_t* u;     // [cpad, ldg] bf16, written; nullptr: not stored (the loss alone)
   uint32_t* counter;
   uint32_t* err;
   int num_sms;

@@ -10,8 +10,9 @@
 //   pass 1     z = h_c W^T for one token chunk (M = chunk rows, N = V, K = d);
 //              the epilogue turns each 128 x 128 quarter of the fp32
 //              accumulator into logsumexp statistics (block max, sum of
-//              exponentials, teacher-weighted logit sum) and stores the
-//              normalised exponentials u = 2^(s2 - m2) as bf16;
+//              exponentials, teacher-weighted logit sum) and, when the
+//              gradients follow, stores the normalised exponentials
+//              u = 2^(s2 - m2) as bf16;
 //   backward   grad_h rows of the chunk = G_c W   (M = chunk, N = d, K = V) and
 //              grad_W (+)= G_c^T h_c              (M = V, N = d, K = chunk),
 //              both in the same launch, fp32 results stored or accumulated
@@ -549,9 +550,10 @@ __device__ void epilogue_store(const KParams& P, const Sizes& S, Ctl* ctl, uint3
 
 // Logsumexp statistics of 32 consecutive logits of one row, in base-2 units
 // s2 = z * k2 relative to the block max m2; exponentials stored as bf16.
+// (u == nullptr: the loss alone, nothing is stored)
 template <bool kMasked>
 __device__ __forceinline__ void lse_chunk32(const float (&v)[32], int nvalid, float k2, float m2,
-                                            float& l, uint16_t* dst) {
+                                            float& l, uint16_t* u, int64_t off) {
   uint32_t w[16];
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
@@ -564,7 +566,8 @@ __device__ __forceinline__ void lse_chunk32(const float (&v)[32], int nvalid, fl
     l += e0 + e1;
     w[j] = pack_bf16x2(e0, e1);
   }
-  uint4* d4 = reinterpret_cast<uint4*>(dst);
+  if (u == nullptr) return;
+  uint4* d4 = reinterpret_cast<uint4*>(u + off);
 #pragma unroll
   for (int j = 0; j < 4; ++j) d4[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
 }
@@ -652,25 +655,25 @@ __device__ void epilogue_pass1(const KParams& P, const Sizes& S, Ctl* ctl, uint3
 
     if (live) {
       const int nv = min(128, P.V - col0);
-      uint16_t* dst = P.u + static_cast<int64_t>(i) * P.ldg + col0;
+      const int64_t off = static_cast<int64_t>(i) * P.ldg + col0;
       float l = 0.f;
       float m2;
       if (nv == 128) {
         const float mx = fmaxf(fmaxf(max32(v0, 32, false), max32(v1, 32, false)),
                                fmaxf(max32(v2, 32, false), max32(v3, 32, false)));
         m2 = mx * k2;
-        lse_chunk32<false>(v0, 32, k2, m2, l, dst);
-        lse_chunk32<false>(v1, 32, k2, m2, l, dst + 32);
-        lse_chunk32<false>(v2, 32, k2, m2, l, dst + 64);
-        lse_chunk32<false>(v3, 32, k2, m2, l, dst + 96);
+        lse_chunk32<false>(v0, 32, k2, m2, l, P.u, off);
+        lse_chunk32<false>(v1, 32, k2, m2, l, P.u, off + 32);
+        lse_chunk32<false>(v2, 32, k2, m2, l, P.u, off + 64);
+        lse_chunk32<false>(v3, 32, k2, m2, l, P.u, off + 96);
       } else {
         const float mx = fmaxf(fmaxf(max32(v0, nv, true), max32(v1, nv - 32, true)),
                                fmaxf(max32(v2, nv - 64, true), max32(v3, nv - 96, true)));
         m2 = mx * k2;
-        lse_chunk32<true>(v0, nv, k2, m2, l, dst);
-        lse_chunk32<true>(v1, nv - 32, k2, m2, l, dst + 32);
-        lse_chunk32<true>(v2, nv - 64, k2, m2, l, dst + 64);
-        lse_chunk32<true>(v3, nv - 96, k2, m2, l, dst + 96);
+        lse_chunk32<true>(v0, nv, k2, m2, l, P.u, off);
+        lse_chunk32<true>(v1, nv - 32, k2, m2, l, P.u, off + 32);
+        lse_chunk32<true>(v2, nv - 64, k2, m2, l, P.u, off + 64);
+        lse_chunk32<true>(v3, nv - 96, k2, m2, l, P.u, off + 96);
       }
       const int64_t o = static_cast<int64_t>(pb) * P.cpad + i;
       P.part_m[o] = m2;
