@@ -335,11 +335,11 @@ def run_builder(args):
     cpu = None
     if not args.no_cpu_baseline:
         import oracle
-        rows = min(64, N)
+        rows = min(512, N)  # about 12 s on 16 host cores at V = 201,088
         hh = x.h_f32()[:rows].astype(np.float64)
         WW = x.W_f32().astype(np.float64)
         t0 = time.perf_counter()
-        oracle.topk_cache(hh, WW, K, block_rows=rows)
+        oracle.topk_cache(hh, WW, K, block_rows=min(rows, 128))
         dtc = time.perf_counter() - t0
         cpu = {"value": rows / dtc, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
                "sample": f"fp64 oracle top-{K} cache of the first {rows} of {N} positions "
@@ -473,10 +473,11 @@ def run_full_teacher(args):
     cpu = None
     if not args.no_cpu_baseline:
         import oracle
-        rows = min(64, N)
+        rows = min(768, N)
         t0 = time.perf_counter()
         oracle.full_kl_fwd_bwd(xs.h_f32()[:rows], xs.W_f32(), xt.h_f32()[:rows], xt.W_f32(),
-                               None if xs.mask is None else xs.mask[:rows], xs.T, block_rows=rows)
+                               None if xs.mask is None else xs.mask[:rows], xs.T,
+                               block_rows=min(rows, 256))
         dtc = time.perf_counter() - t0
         cpu = {"value": rows / dtc, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
                "sample": f"fp64 oracle fwd+bwd of the first {rows} of {N} tokens ({dtc:.1f} s)"}
@@ -654,8 +655,9 @@ def main():
     ap.add_argument("--chunk", type=int, default=0)
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the token count (smaller cases for profiling)")
-    ap.add_argument("--cpu-rows", type=int, default=512,
-                    help="tokens in the CPU-oracle baseline sample")
+    ap.add_argument("--cpu-rows", type=int, default=1536,
+                    help="tokens in the CPU-oracle baseline sample (about 15 s of fp64 "
+                         "fwd+bwd on 16 host cores at the default workload)")
     ap.add_argument("--ref-rows", type=int, default=64,
                     help="tokens per step of the reference (oracle) arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -854,7 +856,8 @@ def main():
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        rows = min(args.cpu_rows, N)
+        # the loss alone costs the oracle about a third of fwd+bwd
+        rows = min(args.cpu_rows * (3 if args.fwd else 1), N)
         dtc, cores = cpu_oracle_time(x, rows, grads=not args.fwd)
         what = "fwd" if args.fwd else "fwd+bwd"
         cpu = {"value": rows / dtc, "unit": "tokens/s", "cores": cores, "kind": "oracle",
