@@ -100,6 +100,16 @@ typedef enum { KD_BF16 = 0, KD_FP32 = 1 } kd_dtype;
 size_t kd_topk_kl_workspace_bytes(int64_t N, int64_t d, int64_t V, int32_t K, int64_t chunk,
                                   kd_dtype dtype);
 
+/*
+ * Bytes of workspace kd_topk_kl_fwd (the loss alone) needs: the same layout
+ * without the chunk's vocabulary-wide exponential tile, which only the
+ * gradients use -- O(N K + chunk V / 64) instead of O(N K + chunk V).  A
+ * workspace of kd_topk_kl_workspace_bytes serves both calls.  Returns 0 for
+ * invalid sizes.
+ */
+size_t kd_topk_kl_fwd_workspace_bytes(int64_t N, int64_t d, int64_t V, int32_t K, int64_t chunk,
+                                      kd_dtype dtype);
+
 /* The chunk (in tokens) used when a call passes chunk <= 0. */
 int64_t kd_topk_kl_default_chunk(int64_t N, int64_t d, int64_t V, kd_dtype dtype);
 
@@ -124,7 +134,8 @@ kd_status kd_topk_kl_fwd_bwd(const void* h, const void* W, kd_dtype dtype,
                              void* workspace, size_t ws_bytes, uint32_t* dev_err_flags,
                              cudaStream_t stream);
 
-/* The loss alone (same definition and arguments, no gradient outputs). */
+/* The loss alone (same definition and arguments, no gradient outputs); its
+ * workspace need only be kd_topk_kl_fwd_workspace_bytes long. */
 kd_status kd_topk_kl_fwd(const void* h, const void* W, kd_dtype dtype, const int32_t* topk_idx,
                          const float* topk_logit, const uint8_t* mask, int64_t N, int64_t d,
                          int64_t V, int32_t K, float T, int64_t chunk, float* loss,

@@ -52,8 +52,13 @@ def test_workspace_plan_is_linear_in_chunk_not_in_n_times_v(lib):
     lay = kd.workspace_layout(32768, d, V, K, c)
     assert lay.chunk == c and lay.chunk_pad == c and lay.n_pb == (V + 127) // 128
     offs = [getattr(lay, f[0]) for f in kd.WorkspaceLayout._fields_ if f[0].startswith("off_")]
-    assert all(o % 256 == 0 for o in offs)
-    assert offs == sorted(offs) and lay.total >= offs[-1]
+    assert all(o % 256 == 0 for o in offs) and len(set(offs)) == len(offs)
+    assert lay.total > max(offs)
+    # the chunk's exponential tile comes last, so the loss alone stops before it
+    assert lay.off_g == max(offs)
+    assert lay.total - lay.off_g == c * ((V + 255) // 256 * 256) * 2
+    fwd = kd.workspace_bytes(32768, d, V, K, c, loss_only=True)
+    assert fwd == lay.off_g and fwd < a / 10
 
 
 def test_default_chunk_splits_evenly(lib):

@@ -33,7 +33,8 @@ STATUS = {0: "KD_OK", 1: "KD_ERR_INVALID_ARG", 2: "KD_ERR_UNSUPPORTED", 3: "KD_E
           4: "KD_ERR_CUDA"}
 
 # Every symbol the headers declare.
-EXPORTS = ["kd_topk_kl_workspace_bytes", "kd_topk_kl_default_chunk", "kd_topk_kl_fwd_bwd",
+EXPORTS = ["kd_topk_kl_workspace_bytes", "kd_topk_kl_fwd_workspace_bytes",
+           "kd_topk_kl_default_chunk", "kd_topk_kl_fwd_bwd",
            "kd_topk_kl_fwd", "kd_status_string", "kd_topk_kl_workspace_layout",
            "kd_umma_gemm_bf16", "kd_timing_enable", "kd_timing_collect",
            "kd_topk_kl_fwd_bwd_noalloc", "kd_topk_cache_workspace_bytes",
@@ -78,6 +79,8 @@ def load_library(path: str = LIB_PATH):
     sz = ctypes.c_size_t
     lib.kd_topk_kl_workspace_bytes.argtypes = [i64, i64, i64, i32, i64, ctypes.c_int]
     lib.kd_topk_kl_workspace_bytes.restype = sz
+    lib.kd_topk_kl_fwd_workspace_bytes.argtypes = [i64, i64, i64, i32, i64, ctypes.c_int]
+    lib.kd_topk_kl_fwd_workspace_bytes.restype = sz
     lib.kd_topk_kl_default_chunk.argtypes = [i64, i64, i64, ctypes.c_int]
     lib.kd_topk_kl_default_chunk.restype = i64
     lib.kd_topk_kl_workspace_layout.argtypes = [i64, i64, i64, i32, i64, ctypes.c_int,
@@ -148,8 +151,12 @@ def _stream_handle(stream) -> int:
     return s.cuda_stream
 
 
-def workspace_bytes(N: int, d: int, V: int, K: int, chunk: int = 0, dtype: int = KD_BF16) -> int:
-    n = load_library().kd_topk_kl_workspace_bytes(N, d, V, K, chunk, dtype)
+def workspace_bytes(N: int, d: int, V: int, K: int, chunk: int = 0, dtype: int = KD_BF16,
+                    loss_only: bool = False) -> int:
+    """Workspace bytes of kd_topk_kl_fwd_bwd, or with loss_only of kd_topk_kl_fwd."""
+    lib = load_library()
+    f = lib.kd_topk_kl_fwd_workspace_bytes if loss_only else lib.kd_topk_kl_workspace_bytes
+    n = f(N, d, V, K, chunk, dtype)
     if n == 0:
         raise KDError(1, "kd_topk_kl_workspace_bytes")
     return int(n)
@@ -188,9 +195,9 @@ def _validate(h, W, idx, logit, mask):
     return N, d, V, idx.shape[1]
 
 
-def allocate_workspace(N, d, V, K, chunk=0, dtype=KD_BF16, device=None):
+def allocate_workspace(N, d, V, K, chunk=0, dtype=KD_BF16, device=None, loss_only=False):
     import torch
-    n = workspace_bytes(N, d, V, K, chunk, dtype)
+    n = workspace_bytes(N, d, V, K, chunk, dtype, loss_only)
     return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
 
 
@@ -230,7 +237,7 @@ def kd_topk_kl_fwd(h, W, topk_idx, topk_logit, mask=None, T: float = 1.0, chunk:
     if loss is None:
         loss = torch.empty(1, dtype=torch.float32, device=h.device)
     if workspace is None:
-        workspace = allocate_workspace(N, d, V, K, chunk, dt, h.device)
+        workspace = allocate_workspace(N, d, V, K, chunk, dt, h.device, loss_only=True)
     st = load_library().kd_topk_kl_fwd(
         _ptr(h), _ptr(W), dt, _ptr(topk_idx), _ptr(topk_logit), _ptr(mask), N, d, V, K,
         float(T), int(chunk), _ptr(loss), _ptr(workspace), workspace.numel(), _ptr(err_flags),

@@ -185,8 +185,9 @@ kd_status make_plan(int64_t N, int64_t d, int64_t V, int32_t K, int64_t chunk, k
   L.off_part_ps = take(4 * part);
   L.off_boff = take(2 * (static_cast<size_t>(P.n_pb) + 1) * static_cast<size_t>(P.cpad));
   L.off_hc = take(static_cast<size_t>(P.cpad) * static_cast<size_t>(d) * P.elem);
-  L.off_g = take(static_cast<size_t>(P.cpad) * static_cast<size_t>(P.ldg) * P.elem);
   L.off_sched = take(256);
+  // last: the loss alone stops here (kd_topk_kl_fwd_workspace_bytes)
+  L.off_g = take(static_cast<size_t>(P.cpad) * static_cast<size_t>(P.ldg) * P.elem);
   L.total = o;
   return KD_OK;
 }
@@ -308,7 +309,9 @@ kd_status run(const void* h, const void* W, kd_dtype dtype, const int32_t* topk_
     return KD_ERR_INVALID_ARG;
   if (want_grads && N > 0 && grad_h == nullptr) return KD_ERR_INVALID_ARG;
   if (!aligned16(W) || (N > 0 && !aligned16(h))) return KD_ERR_INVALID_ARG;
-  if (workspace == nullptr || ws_bytes < P.lay.total) return KD_ERR_WORKSPACE;
+  // the loss alone never touches the last region (the chunk's exponential tile)
+  const size_t need = want_grads ? P.lay.total : P.lay.off_g;
+  if (workspace == nullptr || ws_bytes < need) return KD_ERR_WORKSPACE;
   if (!aligned16(workspace)) return KD_ERR_WORKSPACE;
   const int sms = num_sms();
   if (sms <= 0) return KD_ERR_CUDA;
@@ -365,7 +368,7 @@ kd_status run(const void* h, const void* W, kd_dtype dtype, const int32_t* topk_
       KD_LAUNCH(kPass1Gemm, launch_tc_pass1(p1, a, stream));
     } else {
       KD_LAUNCH(kSimtPass1, launch_simt_pass1(static_cast<const float*>(v.hc), static_cast<const float*>(W), d,
-                                a, k2, static_cast<float*>(v.g), stream));
+                                a, k2, want_grads ? static_cast<float*>(v.g) : nullptr, stream));
     }
     KD_LAUNCH(kLseCombine, launch_lse(a, v.plogp, v.psum, T, v.lse, v.loss_rows, stream));
     if (!want_grads) continue;
@@ -429,6 +432,13 @@ size_t kd_topk_kl_workspace_bytes(int64_t N, int64_t d, int64_t V, int32_t K, in
   kd::Plan p;
   if (kd::make_plan(N, d, V, K, chunk, dtype, &p) != KD_OK) return 0;
   return p.lay.total;
+}
+
+size_t kd_topk_kl_fwd_workspace_bytes(int64_t N, int64_t d, int64_t V, int32_t K, int64_t chunk,
+                                      kd_dtype dtype) {
+  kd::Plan p;
+  if (kd::make_plan(N, d, V, K, chunk, dtype, &p) != KD_OK) return 0;
+  return p.lay.off_g;
 }
 
 int64_t kd_topk_kl_default_chunk(int64_t N, int64_t d, int64_t V, kd_dtype dtype) {

@@ -611,7 +611,7 @@ __global__ void zero_invalid_rows_kernel(const int32_t* __restrict__ row_ok, int
 
 // Pass 1 on CUDA cores: a 32-row x 128-column tile of z = h_c W^T in fp32 FMA,
 // then the same per-block statistics and stored exponentials as the tensor
-// path (fp32 storage).
+// path (fp32 storage; u == nullptr: nothing stored, the loss alone).
 constexpr int kSimtRows = 32;
 constexpr int kSimtKc = 32;
 
@@ -675,11 +675,11 @@ __global__ void __launch_bounds__(256) simt_pass1_kernel(const float* __restrict
     mx = warp_max(mx);
     const float m2 = mx * k2;
     float l = 0.f;
-    float* urow = u + static_cast<int64_t>(i) * a.ldg + col0;
+    float* urow = u != nullptr ? u + static_cast<int64_t>(i) * a.ldg + col0 : nullptr;
     for (int c = tx; c < kPB; c += 32) {
       const float e = (c < nv) ? ex2_approx(fmaf(sZ[li][c], k2, -m2)) : 0.f;
       l += e;
-      urow[c] = e;
+      if (urow != nullptr) urow[c] = e;
     }
     l = warp_sum(l);
     float ps = 0.f;
