@@ -197,3 +197,17 @@ def test_product_path_fails_loudly_without_the_library(tmp_path):
     assert len(lines) == 2, r.stdout + r.stderr
     assert lines[0].startswith("RuntimeError") and "is missing" in lines[0], lines[0]
     assert lines[1].startswith("ValueError") and "CUDA tensor" in lines[1], lines[1]
+
+
+def test_workspace_size_checks_of_the_two_calls(lib):
+    # Host-side rejections only (they return before any CUDA call): the loss
+    # alone needs kd_topk_kl_fwd_workspace_bytes, fwd+bwd the full size.
+    N, d, V, K = 64, 16, 1000, 4
+    full = kd.workspace_bytes(N, d, V, K)
+    fwd = kd.workspace_bytes(N, d, V, K, loss_only=True)
+    assert 0 < fwd < full
+    assert call_fwd_bwd(lib, N=N, d=d, V=V, K=K, ws=256, ws_bytes=fwd) == 3
+    assert call_fwd_bwd(lib, N=N, d=d, V=V, K=K, ws=256, ws_bytes=full - 1) == 3
+    st = lib.kd_topk_kl_fwd(16, 16, kd.KD_BF16, 16, 16, None, N, d, V, K, 1.0, 0, 16, 256,
+                            fwd - 1, None, None)
+    assert st == 3
