@@ -98,7 +98,8 @@ def full_kl_grad_logits(h_s, W_s, h_t, W_t, mask, T):
 
 def full_kl_sampled_rows(h_s, W_s, h_t, W_t, mask, T, rows):
     """Per-row results of the full loss for the given rows only: loss_rows,
-    lse_s and grad_h rows, with N_valid over the whole batch."""
+    lse_s and grad_h rows, with N_valid over the whole batch.  Masked rows
+    give a zero loss term and a zero grad_h row, as in full_kl_fwd_bwd."""
     valid = (np.ones(np.asarray(h_s).shape[0], dtype=bool) if mask is None
              else np.asarray(mask) != 0)
     n_valid = int(valid.sum())
@@ -119,4 +120,5 @@ def full_kl_sampled_rows(h_s, W_s, h_t, W_t, mask, T, rows):
     grad_h = G @ Ws
     v = valid[rows]
     grad_h[~v] = 0.0
+    loss_rows[~v] = 0.0
     return dict(loss_rows=loss_rows, lse_s=lse_s, grad_h=grad_h, valid=v, n_valid=n_valid)

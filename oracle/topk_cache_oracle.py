@@ -62,17 +62,6 @@ def topk_cache(h, W, K, block_rows=256):
     return idx, val
 
 
-def logits_at(h, W, rows, cols):
-    """z[rows[i], cols[i, k]] in float64 (for checking selected entries of a
-    large problem one row at a time)."""
-    h = np.asarray(h, dtype=np.float64)
-    W = np.asarray(W, dtype=np.float64)
-    out = np.zeros(cols.shape, dtype=np.float64)
-    for i, r in enumerate(rows):
-        out[i] = W[cols[i]] @ h[r]
-    return out
-
-
 def row_logits(h, W, rows):
     """Full logit rows z[rows, :] in float64."""
     h = np.asarray(h, dtype=np.float64)

@@ -135,7 +135,8 @@ def test_sampled_rows_match_the_full_computation():
     s = fko.full_kl_sampled_rows(hs, Ws, ht, Wt, mask, 2.0, rows)
     np.testing.assert_allclose(s["grad_h"], r["grad_h"][rows], rtol=1e-12, atol=1e-15)
     v = s["valid"]
-    np.testing.assert_allclose(s["loss_rows"][v], r["loss_rows"][rows][v], rtol=1e-12)
+    np.testing.assert_allclose(s["loss_rows"], r["loss_rows"][rows], rtol=1e-12)
+    assert np.all(s["loss_rows"][~v] == 0) and np.all(s["grad_h"][~v] == 0)
     np.testing.assert_allclose(s["lse_s"][v], r["lse_s"][rows][v], rtol=1e-12)
 
 

@@ -114,6 +114,27 @@ def test_k_equal_v_is_a_full_ranking():
         assert np.all(np.diff(v[r]) <= 0)
 
 
+def test_row_logits_match_plain_loops_and_the_selected_values():
+    # row_logits (used to check full-size cache rows one row at a time) is
+    # the same product as the cache's logits: with small integers every dot
+    # product is exact, so plain Python loops give the very same numbers, and
+    # at the selected indices the rows hold the cache's own values
+    rng = np.random.default_rng(11)
+    h = rng.integers(-3, 4, size=(9, 6)).astype(np.float64)
+    W = rng.integers(-3, 4, size=(41, 6)).astype(np.float64)
+    rows = np.array([8, 0, 5, 5])
+    Z = oracle.row_logits(h, W, rows)
+    assert Z.shape == (4, 41)
+    for i, r in enumerate(rows):
+        for v in range(41):
+            s = 0
+            for k in range(6):
+                s += int(h[r, k]) * int(W[v, k])
+            assert Z[i, v] == s
+    idx, val = oracle.topk_cache(h, W, 7)
+    np.testing.assert_array_equal(np.take_along_axis(Z, idx[rows], axis=1), val[rows])
+
+
 def test_nan_logits_rank_last():
     assert oracle.rank_order([1.0, np.nan, 5.0, np.nan, -np.inf]).tolist() == [2, 0, 4, 1, 3]
     with pytest.raises(ValueError):
