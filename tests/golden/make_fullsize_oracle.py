@@ -1,0 +1,108 @@
+"""Writes the fp64 oracle's results for the full-size workloads into a local
+cache that the full-size GPU parity tests read.
+
+At 32K and 128K tokens with a 201,088-word vocabulary the dense fp64 forward
+takes minutes to tens of minutes of host time (2 N d V multiply-adds), too long
+to repeat inside every test run, so it is computed once per input set and kept
+in tests/.oracle_cache/ (not under version control: it is a few MB of binary
+arrays and is rebuilt from the oracle and the seeded generator alone).
+
+Every value stored here comes from oracle/ and the seeded input generator
+(synth), never from the CUDA path.  Per workload:
+  * the whole-batch loss, N_valid, and every token's lse and loss term (the
+    oracle's full forward, rows processed in blocks);
+  * about 200 rows of grad_W (half the vocabulary rows of teacher entries of
+    rank 1, half uniform, plus the first and the last row), each computed from
+    the oracle's own lse.
+Each file carries a digest of the inputs it was computed from; a test that
+finds a different digest recomputes.
+
+    python tests/golden/make_fullsize_oracle.py [config ...]     (default: 3 5 4)
+"""
+import hashlib
+import os
+import sys
+import time
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(os.path.dirname(HERE))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+CACHE_DIR = os.path.join(ROOT, "tests", ".oracle_cache")
+
+
+def input_digest(x) -> str:
+    """SHA-256 over the exact bits of one synthetic problem's inputs."""
+    d = hashlib.sha256()
+    for a in (x.h, x.W, x.idx, x.logit):
+        d.update(np.ascontiguousarray(a).view(np.uint8).data)
+    d.update(b"nomask" if x.mask is None else np.ascontiguousarray(x.mask).data)
+    d.update(repr((x.dtype, x.T, x.N, x.d, x.V, x.K)).encode())
+    return d.hexdigest()
+
+
+def vocab_sample(x, n_teacher=100, n_uniform=100, seed=None) -> np.ndarray:
+    """Vocabulary rows to check in grad_W: the rank-1 teacher index of
+    n_teacher random tokens, n_uniform uniform rows, and rows 0 and V - 1."""
+    rng = np.random.default_rng(1000 + x.seed if seed is None else seed)
+    toks = rng.choice(x.N, size=min(n_teacher, x.N), replace=False)
+    teach = x.idx[toks, 0].astype(np.int64)
+    uni = rng.integers(0, x.V, size=n_uniform)
+    return np.unique(np.concatenate([teach, uni, [0, x.V - 1]]))
+
+
+def cache_path(cfg: int) -> str:
+    return os.path.join(CACHE_DIR, f"config{cfg}.npz")
+
+
+def compute(x, block_rows=512, log=None):
+    """The oracle's whole-batch forward and sampled grad_W rows for x."""
+    import oracle
+    t0 = time.time()
+    h = x.h_f32()
+    W = x.W_f32()
+    full = oracle.fwd(h, W, x.idx, x.logit, x.mask, x.T, block_rows=block_rows)
+    t1 = time.time()
+    vr = vocab_sample(x)
+    gW = oracle.grad_W_rows(h, W, x.idx, x.logit, x.mask, x.T, vr, full["lse"])
+    t2 = time.time()
+    if log is not None:
+        log(f"{x.name}: forward {t1 - t0:.0f} s, {vr.size} grad_W rows {t2 - t1:.0f} s")
+    return dict(digest=np.array(input_digest(x)), loss=np.float64(full["loss"]),
+                n_valid=np.int64(full["n_valid"]), lse=full["lse"],
+                loss_rows=full["loss_rows"], vocab_rows=vr, grad_W_rows=gW)
+
+
+def load_or_compute(cfg: int, x, log=None):
+    """The cached oracle results for config cfg if they match x's inputs, else
+    computed now (and cached)."""
+    path = cache_path(cfg)
+    dig = input_digest(x)
+    if os.path.exists(path):
+        with np.load(path) as z:
+            if str(z["digest"]) == dig:
+                return {k: z[k] for k in z.files}
+    res = compute(x, log=log)
+    os.makedirs(CACHE_DIR, exist_ok=True)
+    tmp = path + f".tmp{os.getpid()}.npz"
+    np.savez(tmp, **res)
+    os.replace(tmp, path)
+    return res
+
+
+def main(argv):
+    from top_kl_loss_token_b300 import synth
+    cfgs = [int(a) for a in argv] or [3, 5, 4]
+    for cfg in cfgs:
+        x = synth.make_config(cfg)
+        res = load_or_compute(cfg, x, log=lambda s: print(s, flush=True))
+        print(f"config {cfg}: loss {float(res['loss']):.9f}, N_valid {int(res['n_valid'])}, "
+              f"{res['vocab_rows'].size} grad_W rows -> {cache_path(cfg)}", flush=True)
+        del x, res
+
+
+if __name__ == "__main__":
+    main(sys.argv[1:])

@@ -4,9 +4,26 @@ running the library, and the parity tolerances.
 Tolerances (fixed by the target): bf16 inputs -> loss relative error <= 1e-3
 and gradient max-abs error <= 2e-2 * max|gradient|; fp32 inputs -> 1e-5 and
 1e-4."""
+import importlib.util
+import os
+
 import numpy as np
 
 TOL = {"bf16": (1e-3, 2e-2), "fp32": (1e-5, 1e-4)}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def fullsize_oracle(cfg, x):
+    """The fp64 oracle's whole-batch forward (loss, every lse and loss term)
+    and sampled grad_W rows for full-size config cfg, from the local cache
+    that tests/golden/make_fullsize_oracle.py writes (computed now, and
+    cached, when it is missing or was made from other inputs)."""
+    spec = importlib.util.spec_from_file_location(
+        "make_fullsize_oracle", os.path.join(_HERE, "golden", "make_fullsize_oracle.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod.load_or_compute(cfg, x)
 
 
 def to_device(x, device="cuda"):

@@ -1,0 +1,76 @@
+"""The whole-matrix checks that the full-size GPU tests apply to grad_W and
+grad_h (tests/test_gpu_fullsize.py), run here on the CPU against the fp64
+oracle: they must pass on exact results and on results whose dL/dz tile
+carries the two bf16 roundings of the GPU path, and they must fail on planted
+mistakes (the teacher term of dL/dz left out; one 256-row tile of grad_W, or
+one 128-row tile of grad_h, missing)."""
+import numpy as np
+import pytest
+
+import oracle
+from top_kl_loss_token_b300 import synth
+from test_gpu_fullsize import check_projection_identity, check_sum_rule
+
+
+def _bf16(a):
+    return synth.bf16_bits_to_f32(synth.bf16_bits(np.asarray(a, np.float32))).astype(np.float64)
+
+
+@pytest.fixture(scope="module")
+def problem():
+    x = synth.make_inputs(2048, 64, 3000, 16, T=2.0, dtype="bf16", seed=31, mask="random0.1")
+    g = oracle.grad_logits(x.h_f32(), x.W_f32(), x.idx, x.logit, x.mask, x.T)
+    G = g["G"]
+    tn = x.T * g["n_valid"]
+    # dL/dz as the GPU stores it: the softmax rounded to bf16 (the stored
+    # exponential), then the tile G rounded to bf16
+    q = np.where(g["valid"][:, None], np.exp(
+        (x.h_f32().astype(np.float64) @ x.W_f32().astype(np.float64).T) / x.T
+        - g["lse"][:, None]), 0.0)
+    q = np.nan_to_num(q)
+    Gq = _bf16(_bf16(q) / tn + (G - q / tn))
+    return x, g, G, Gq
+
+
+def _outputs(x, G, n_valid):
+    h = x.h_f32().astype(np.float64)
+    W = x.W_f32().astype(np.float64)
+    valid = np.ones(x.N, bool) if x.mask is None else x.mask != 0
+    return dict(grad_W=G.T @ np.where(valid[:, None], h, 0.0), grad_h=G @ W, n_valid=n_valid)
+
+
+def test_checks_pass_on_exact_and_on_rounded_results(problem):
+    x, g, G, Gq = problem
+    exact = _outputs(x, G, g["n_valid"])
+    assert check_sum_rule(x, exact) < 0.05
+    assert check_projection_identity(x, exact) < 1e-12
+    rounded = _outputs(x, Gq, g["n_valid"])
+    assert check_sum_rule(x, rounded) <= 1.0
+    check_projection_identity(x, rounded)
+
+
+def test_sum_rule_catches_a_missing_teacher_term(problem):
+    x, g, G, Gq = problem
+    # dL/dz without the teacher's subtraction: the softmax term alone
+    valid = np.ones(x.N, bool) if x.mask is None else x.mask != 0
+    p_scat = np.zeros_like(G)
+    r = np.repeat(np.arange(x.N), x.K)
+    np.add.at(p_scat, (r, x.idx.reshape(-1).astype(np.int64)), g["p"].reshape(-1))
+    no_teacher = G + p_scat / (x.T * g["n_valid"]) * valid[:, None]
+    with pytest.raises(AssertionError):
+        check_sum_rule(x, _outputs(x, no_teacher, g["n_valid"]))
+
+
+def test_projection_identity_catches_a_missing_tile(problem):
+    x, g, G, Gq = problem
+    out = _outputs(x, Gq, g["n_valid"])
+    bad = dict(out)
+    bad["grad_W"] = out["grad_W"].copy()
+    bad["grad_W"][512:768] = 0.0
+    with pytest.raises(AssertionError):
+        check_projection_identity(x, bad)
+    bad = dict(out)
+    bad["grad_h"] = out["grad_h"].copy()
+    bad["grad_h"][1024:1152] = 0.0
+    with pytest.raises(AssertionError):
+        check_projection_identity(x, bad)
