@@ -147,11 +147,10 @@ kd_status kd_topk_kl_fwd(const void* h, const void* W, kd_dtype dtype, const int
  * allocate device memory.  (The write-ups have no counterpart: this is an
  * interface convenience, not part of the method.)
  *
- * Who needs it: code that may not call cudaMalloc -- a region being captured
- * into a CUDA graph, a process whose memory pool owns the device and forbids
- * allocations beside it, a plug-in that is handed device pointers for its
- * inputs and outputs but no allocator -- still has to supply the workspace
- * that kd_topk_kl_fwd_bwd takes.  This call uses instead a scratch array of
+ * Who needs it: code that may not call cudaMalloc -- a process whose memory
+ * pool owns the device and forbids allocations beside it, a plug-in that is
+ * handed device pointers for its inputs and outputs but no allocator -- still
+ * has to supply the workspace that kd_topk_kl_fwd_bwd takes.  This call uses instead a scratch array of
  * KD_NOALLOC_SCRATCH_BYTES that the library holds in device memory: every GPU
  * that loads the library keeps that array until the process exits.  The call
  * itself allocates nothing (no cudaMalloc, cudaFree or allocating library

@@ -1,15 +1,16 @@
 """kd_topk_kl_fwd_bwd_noalloc, the entry point for callers that cannot
-allocate device memory (a region being captured into a CUDA graph, a process
-whose memory pool owns the device, a plug-in that is handed device pointers but
-no allocator).  It runs the same kernels as kd_topk_kl_fwd_bwd with its
-workspace in a fixed scratch array that the library holds, so its results must
-agree with the ordinary call, and a second call must not be disturbed by what
-the first one left in that shared array.
+allocate device memory (a process whose memory pool owns the device, a plug-in
+that is handed device pointers but no allocator).  It runs the same kernels as
+kd_topk_kl_fwd_bwd with its workspace in a fixed scratch array that the
+library holds, so its results must agree with the ordinary call and with the
+fp64 oracle, and a second call must not be disturbed by what the first one left
+in that shared array.
 
 This file is named so that pytest collects it last."""
 import numpy as np
 import pytest
 
+import oracle
 import top_kl_loss_token_b300 as kd_mod
 from top_kl_loss_token_b300 import synth
 from kd_testutil import TOL, max_rel_err, to_device
@@ -59,6 +60,12 @@ def _assert_close(ref, got, dtype):
     assert max_rel_err(got[2], ref[2]) <= tg
 
 
+def _assert_oracle(x, got):
+    """The no-alloc results against the fp64 dense definition."""
+    r = oracle.fwd_bwd(x.h_f32(), x.W_f32(), x.idx, x.logit, x.mask, x.T)
+    _assert_close((r["loss"], r["grad_h"], r["grad_W"]), got, x.dtype)
+
+
 @pytest.mark.gpu
 def test_noalloc_matches_fwd_bwd_on_two_calls_in_a_row(kd):
     # first call: ragged vocabulary (3000 = 23.4 blocks of 128), 5 row tiles,
@@ -66,8 +73,10 @@ def test_noalloc_matches_fwd_bwd_on_two_calls_in_a_row(kd):
     a = synth.make_inputs(640, 256, 3000, 16, T=2.0, dtype="bf16", seed=211, mask="random0.15")
     ref_a, got_a = _reference_and_noalloc(kd, a, 0)
     _assert_close(ref_a, got_a, "bf16")
+    _assert_oracle(a, got_a)
     # second call, straight after, on the same scratch array: other sizes, no
     # mask, three chunks of 128 tokens with a short last one
     b = synth.make_inputs(300, 128, 1000, 8, T=1.0, dtype="bf16", seed=212)
     ref_b, got_b = _reference_and_noalloc(kd, b, 128)
     _assert_close(ref_b, got_b, "bf16")
+    _assert_oracle(b, got_b)

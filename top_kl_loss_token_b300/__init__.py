@@ -259,6 +259,8 @@ def kd_topk_kl_fwd_bwd_noalloc(h, W, topk_idx, topk_logit, loss, grad_h, grad_W,
         if (not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != shape
                 or t.element_size() != 4 or not t.is_floating_point()):
             raise ValueError(f"{name} must be a contiguous fp32 CUDA tensor of shape {shape}")
+        if t.device != h.device:
+            raise ValueError(f"{name} is on {t.device}, the inputs on {h.device}")
     st = load_library().kd_topk_kl_fwd_bwd_noalloc(
         _ptr(h), _ptr(W), dt, _ptr(topk_idx), _ptr(topk_logit), _ptr(mask), N, d, V, K,
         float(T), int(chunk), _ptr(loss), _ptr(grad_h), _ptr(grad_W), _ptr(err_flags),

@@ -2,12 +2,11 @@
 // workspace in a fixed device array that the library owns, for callers that
 // cannot allocate device memory themselves.
 //
-// Some callers can't call cudaMalloc: code that runs while a CUDA graph is
-// being captured (an allocation there is an error or is left out of the
-// graph), allocators that forbid raw cudaMalloc next to their own pool, and
-// plug-ins or embedded runtimes that are handed device pointers for their
-// inputs and outputs but no allocator.  This entry point lets them run the
-// loss anyway, up to a fixed size.
+// Some callers can't call cudaMalloc: processes whose caching allocator owns
+// the device memory and forbids raw cudaMalloc beside its pool, and plug-ins
+// or embedded runtimes that are handed device pointers for their inputs and
+// outputs but no allocator.  This entry point lets them run the loss anyway,
+// up to a fixed size.
 //
 // The scratch array is a file-scope __device__ array; in host code its name is
 // only a stand-in, so its device address is looked up with
