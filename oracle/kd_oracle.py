@@ -115,19 +115,25 @@ def _row_block(H, W, idx, p, valid, T, n_valid):
     return lse, loss_rows, G
 
 
-def fwd_bwd(h, W, topk_idx, topk_logit, mask, T, block_rows=256, want_grads=True):
+def fwd_bwd(h, W, topk_idx, topk_logit, mask, T, block_rows=256, want_grads=True, n_norm=None):
     """Dense loss, grad_h and grad_W in float64.
 
     h [N,d], W [V,d] are the exact values the kernels see (bf16 or fp32
     widened to float64).  Returns a dict with loss, grad_h, grad_W, lse,
     loss_rows, valid, n_valid, flags.  Rows are processed in blocks of
-    block_rows; the result does not depend on that size beyond rounding."""
+    block_rows; the result does not depend on that size beyond rounding.
+
+    n_norm: the divisor of the mean, N_valid of these rows by default.  When
+    a batch is split into token shards, the batch's loss is still the mean
+    over all of its valid tokens, so each shard divides by the batch's
+    N_valid: the shards' losses and grad_W then add up to the batch's."""
     H = _f64(h)
     Wd = _f64(W)
     N, d = H.shape
     V = Wd.shape[0]
     p, valid, flags = teacher_distribution(topk_idx, topk_logit, mask, V, T)
     n_valid = int(valid.sum())
+    div = n_valid if n_norm is None else int(n_norm)
     lse = np.full(N, np.nan)
     loss_rows = np.zeros(N)
     grad_h = np.zeros((N, d)) if want_grads else None
@@ -138,20 +144,21 @@ def fwd_bwd(h, W, topk_idx, topk_logit, mask, T, block_rows=256, want_grads=True
         v = valid[r0:r1]
         if not v.any():
             continue
-        l_b, lr_b, G = _row_block(H[r0:r1], Wd, idx[r0:r1], p[r0:r1], v, T, n_valid)
+        l_b, lr_b, G = _row_block(H[r0:r1], Wd, idx[r0:r1], p[r0:r1], v, T, div)
         lse[r0:r1] = np.where(v, l_b, np.nan)
         loss_rows[r0:r1] = lr_b
         if want_grads:
             grad_h[r0:r1] = G @ Wd
             grad_W += G.T @ np.where(v[:, None], H[r0:r1], 0.0)
-    loss = float(loss_rows.sum() / n_valid) if n_valid > 0 else 0.0
+    loss = float(loss_rows.sum() / div) if div > 0 else 0.0
     return dict(loss=loss, grad_h=grad_h, grad_W=grad_W, lse=lse, loss_rows=loss_rows,
                 valid=valid, n_valid=n_valid, flags=flags, p=p)
 
 
-def fwd(h, W, topk_idx, topk_logit, mask, T, block_rows=256):
+def fwd(h, W, topk_idx, topk_logit, mask, T, block_rows=256, n_norm=None):
     """Loss only (same definition as fwd_bwd)."""
-    return fwd_bwd(h, W, topk_idx, topk_logit, mask, T, block_rows, want_grads=False)
+    return fwd_bwd(h, W, topk_idx, topk_logit, mask, T, block_rows, want_grads=False,
+                   n_norm=n_norm)
 
 
 def teacher_plogp(p):

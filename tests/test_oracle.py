@@ -331,6 +331,30 @@ def test_no_valid_rows_gives_zero():
     assert np.all(r["grad_h"] == 0) and np.all(r["grad_W"] == 0)
 
 
+def test_token_shards_with_the_batch_divisor_add_up_to_the_batch():
+    # A batch split into token shards: each shard divides by the batch's
+    # N_valid, so the shards' losses and grad_W add up to the batch's and
+    # their grad_h rows are the batch's rows (linearity of the sum over
+    # tokens); the default divisor is the shard's own count.
+    h, W, idx, logit, T = rand_problem(N=9, d=4, V=13, K=3, T=2.0, seed=23)
+    mask = np.array([1, 0, 1, 1, 1, 0, 1, 1, 1], np.uint8)
+    full = oracle.fwd_bwd(h, W, idx, logit, mask, T)
+    parts = [slice(0, 2), slice(2, 7), slice(7, 9)]
+    outs = [oracle.fwd_bwd(h[s], W, idx[s], logit[s], mask[s], T, n_norm=full["n_valid"])
+            for s in parts]
+    assert sum(o["loss"] for o in outs) == pytest.approx(full["loss"], rel=1e-13)
+    np.testing.assert_allclose(sum(o["grad_W"] for o in outs), full["grad_W"], rtol=1e-12,
+                               atol=1e-16)
+    np.testing.assert_allclose(np.concatenate([o["grad_h"] for o in outs]), full["grad_h"],
+                               rtol=1e-12, atol=1e-16)
+    own = oracle.fwd_bwd(h[2:7], W, idx[2:7], logit[2:7], mask[2:7], T)
+    same = oracle.fwd_bwd(h[2:7], W, idx[2:7], logit[2:7], mask[2:7], T, n_norm=own["n_valid"])
+    assert own["loss"] == same["loss"]
+    assert np.array_equal(own["grad_W"], same["grad_W"])
+    zero = oracle.fwd(h[:2], W, idx[:2], logit[:2], np.zeros(2, np.uint8), T, n_norm=0)
+    assert zero["loss"] == 0.0
+
+
 def test_minus_inf_teacher_entry_has_zero_probability():
     h, W, idx, logit, T = rand_problem(N=3, d=3, V=8, K=3, seed=19)
     l2 = logit.copy()
