@@ -14,7 +14,9 @@ grad_h and grad_W products).  Inputs are larger than L2 (W alone is 1.16 GB),
 so no flush is needed between steps.
 
 Under torchrun (N > 1) every rank runs its own token shard of the same size
-(weak scaling, no collective on the data path); the barrier and max-over-ranks
+(weak scaling) as one data-parallel step (fwd_bwd_dp): the ranks' valid-token
+counts are all-reduced before the loss is divided, and loss and grad_W are
+all-reduced after it, inside the timed region; the barrier and max-over-ranks
 time use torch.distributed.  `--impl reference` times the fp64 CPU oracle on a
 bounded sample of the same workload (rank 0 only).
 
@@ -755,8 +757,17 @@ def main():
             kd.fwd(h, W, idx, lg, mask, x.T, chunk, loss=loss, workspace=ws, err_flags=err,
                    stream=stream)
             return
+        if world > 1:
+            # the data-parallel step: counts, loss and grad_W all-reduced
+            kd.fwd_bwd_dp(h, W, idx, lg, mask, x.T, chunk, loss=loss, grad_h=grad_h,
+                          grad_W=grad_W, workspace=ws, err_flags=err, stream=stream)
+            return
         kd.fwd_bwd(h, W, idx, lg, mask, x.T, chunk, loss=loss, grad_h=grad_h, grad_W=grad_W,
                    workspace=ws, err_flags=err, stream=stream)
+
+    def check_flags(where):
+        if int(err.item()) != 0:
+            raise RuntimeError(f"device error flags {int(err.item())} after {where}")
 
     def barrier():
         if world > 1:
@@ -765,8 +776,7 @@ def main():
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
-    if int(err.item()) != 0:
-        raise RuntimeError(f"device error flags {int(err.item())}")
+    check_flags("the warm-up steps")
     peak_extra = (torch.cuda.max_memory_allocated(dev) - base_alloc) / 2 ** 30
 
     # ---------------- timed region: inputs resident in HBM
@@ -785,6 +795,7 @@ def main():
         barrier()
     kd.timing_enable(False)
     kernels = kd.timing_collect()
+    check_flags("the timed steps")
     ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
     tokens_total = N * args.steps * world
     value = tokens_total / (ms / 1000.0)
@@ -815,6 +826,7 @@ def main():
             stream.synchronize()
         e1.record(stream)
         torch.cuda.synchronize(dev)
+    check_flags("the end-to-end steps")
     barrier()
     e_value = N * e_steps * world / (max_over_ranks(e0.elapsed_time(e1), world, dev) / 1000.0)
 
@@ -871,7 +883,8 @@ def main():
         "data": "synthetic",
         "config": {"workload": workload_name(x), "chunk": chunk, "n_chunks": n_chunks,
                    "l2": "inputs larger than L2 (W alone 1.16 GB), no flush",
-                   "parallelism": f"token shards x{world}" if world > 1 else "1 GPU"},
+                   "parallelism": (f"token shards x{world}, counts, loss and grad_W "
+                                   "all-reduced per step") if world > 1 else "1 GPU"},
         "tflops_per_gpu": tflops,
         "pct_of_bf16_peak": {"burst": tflops / peaks["bf16_tflops"],
                              "sustained": tflops / peaks["bf16_tflops_sustained"],

@@ -143,6 +143,57 @@ kd_status kd_topk_kl_fwd(const void* h, const void* W, kd_dtype dtype, const int
                          cudaStream_t stream);
 
 /*
+ * Data parallelism: one batch split over several ranks (processes, one GPU
+ * each).  Every rank owns some of the tokens and their teacher-cache rows; W
+ * is replicated.  The loss of the batch is the mean over ALL its valid tokens
+ * (the token-level mean above, taken over the whole batch), so each rank's
+ * terms must be divided by N_valid of the whole batch, which is known only
+ * once every rank has counted its own valid rows.  Two calls split
+ * kd_topk_kl_fwd_bwd at that point:
+ *   1. kd_topk_kl_prepare     teacher preparation and the valid-row map of
+ *                             this rank's tokens; writes this rank's N_valid
+ *                             to *n_valid (device int64, optional);
+ *   2. (caller)               sums n_valid over the ranks (an all-reduce on
+ *                             the same stream: no host synchronisation);
+ *   3. kd_topk_kl_fwd_bwd_prepared / kd_topk_kl_fwd_prepared
+ *                             the chunk loop over the prepared workspace with
+ *                             the divisor *n_norm (device int64): loss =
+ *                             (sum of this rank's loss terms) / n_norm, and
+ *                             dL/dz = (softmax - p scattered) / (T n_norm).
+ * Summing loss and grad_W over the ranks then gives the batch's loss and
+ * grad_W exactly as one call over the whole batch would; grad_h rows stay
+ * with their rank.  kd_topk_kl_fwd_bwd is step 1 followed by step 3 with
+ * n_norm = this rank's own count.
+ *
+ * The prepared call must use the same sizes (N, d, V, K, chunk, dtype), T and
+ * workspace as the kd_topk_kl_prepare call, be ordered after it (same stream,
+ * or an event), and no other call may use that workspace in between.
+ * n_norm == NULL divides by this rank's own count; *n_norm <= 0 gives a zero
+ * loss and zero gradients (no valid token in the whole batch); *n_norm
+ * smaller than this rank's count is a caller error (the results are scaled
+ * accordingly, nothing is checked).  The prepare call needs a workspace of at
+ * least kd_topk_kl_fwd_workspace_bytes; kd_topk_kl_fwd_bwd_prepared needs
+ * kd_topk_kl_workspace_bytes.  Errors as for kd_topk_kl_fwd_bwd; the data
+ * flags (INDEX_RANGE, BAD_TEACHER) are raised by the prepare call.
+ */
+kd_status kd_topk_kl_prepare(const int32_t* topk_idx, const float* topk_logit,
+                             const uint8_t* mask, int64_t N, int64_t d, int64_t V, int32_t K,
+                             float T, int64_t chunk, kd_dtype dtype, void* workspace,
+                             size_t ws_bytes, int64_t* n_valid, uint32_t* dev_err_flags,
+                             cudaStream_t stream);
+
+kd_status kd_topk_kl_fwd_bwd_prepared(const void* h, const void* W, kd_dtype dtype, int64_t N,
+                                      int64_t d, int64_t V, int32_t K, float T, int64_t chunk,
+                                      const int64_t* n_norm, float* loss, float* grad_h,
+                                      float* grad_W, void* workspace, size_t ws_bytes,
+                                      uint32_t* dev_err_flags, cudaStream_t stream);
+
+kd_status kd_topk_kl_fwd_prepared(const void* h, const void* W, kd_dtype dtype, int64_t N,
+                                  int64_t d, int64_t V, int32_t K, float T, int64_t chunk,
+                                  const int64_t* n_norm, float* loss, void* workspace,
+                                  size_t ws_bytes, uint32_t* dev_err_flags, cudaStream_t stream);
+
+/*
  * kd_topk_kl_fwd_bwd_noalloc -- kd_topk_kl_fwd_bwd for callers that cannot
  * allocate device memory.  (The write-ups have no counterpart: this is an
  * interface convenience, not part of the method.)

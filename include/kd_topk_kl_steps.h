@@ -26,7 +26,8 @@ extern "C" {
  * Where a call with these sizes keeps its intermediates inside the workspace
  * (byte offsets from the workspace base, each 256-byte aligned).  Valid after
  * a kd_topk_kl_fwd_bwd / kd_topk_kl_fwd call has completed on its stream:
- *   ctrl:       uint32 error flags at +0, int32 N_valid at +4, double loss sum at +8
+ *   ctrl:       uint32 error flags at +0, int32 N_valid at +4, double loss sum at +8,
+ *               int64 N_valid at +16
  *   rows:       int32 [N]  original row of the i-th valid row (i < N_valid)
  *   lse:        fp32  [N]  lse_i of the i-th valid row (natural log, of s = z/T)
  *   loss_rows:  fp32  [N]  loss term of the i-th valid row (before the 1/N_valid)
@@ -127,8 +128,10 @@ kd_status kd_umma_gemm_bf16_wait_test(const void* A, const void* B, float* D, in
  * enabled, the library brackets each of its kernel launches with a pair of
  * CUDA events recorded on the launching stream.  kd_timing_collect waits for
  * those events, returns one entry per kernel kind (launch count and summed
- * device time), and clears the record.  Host-side state shared by all calls
- * of the process; not thread-safe; off by default.
+ * device time), and clears the record.  One record for the whole process,
+ * guarded by a lock: calls from several host threads and on several devices
+ * may record at the same time (each event is made on the device of the
+ * stream it brackets); collect returns them all together.  Off by default.
  */
 typedef struct {
   char name[32];      /* kernel kind, e.g. "pass1_gemm", "bwd_gemm"          */

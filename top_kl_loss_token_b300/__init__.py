@@ -40,7 +40,8 @@ EXPORTS = ["kd_topk_kl_workspace_bytes", "kd_topk_kl_fwd_workspace_bytes",
            "kd_topk_kl_fwd_bwd_noalloc", "kd_topk_cache_workspace_bytes",
            "kd_topk_cache_default_chunk", "kd_topk_cache_build", "kd_umma_gemm_bf16_wait_test",
            "kd_full_kl_workspace_bytes", "kd_full_kl_default_chunk", "kd_full_kl_fwd_bwd",
-           "kd_full_kl_workspace_layout"]
+           "kd_full_kl_workspace_layout", "kd_topk_kl_prepare", "kd_topk_kl_fwd_bwd_prepared",
+           "kd_topk_kl_fwd_prepared"]
 
 # Size of the library-held scratch array used by kd_topk_kl_fwd_bwd_noalloc.
 KD_NOALLOC_SCRATCH_BYTES = 64 << 20
@@ -92,6 +93,15 @@ def load_library(path: str = LIB_PATH):
     lib.kd_topk_kl_fwd.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, i64, i64, i64, i32, f32, i64,
                                    vp, vp, sz, vp, vp]
     lib.kd_topk_kl_fwd.restype = ctypes.c_int
+    lib.kd_topk_kl_prepare.argtypes = [vp, vp, vp, i64, i64, i64, i32, f32, i64, ctypes.c_int,
+                                       vp, sz, vp, vp, vp]
+    lib.kd_topk_kl_prepare.restype = ctypes.c_int
+    lib.kd_topk_kl_fwd_bwd_prepared.argtypes = [vp, vp, ctypes.c_int, i64, i64, i64, i32, f32,
+                                                i64, vp, vp, vp, vp, vp, sz, vp, vp]
+    lib.kd_topk_kl_fwd_bwd_prepared.restype = ctypes.c_int
+    lib.kd_topk_kl_fwd_prepared.argtypes = [vp, vp, ctypes.c_int, i64, i64, i64, i32, f32, i64,
+                                            vp, vp, vp, sz, vp, vp]
+    lib.kd_topk_kl_fwd_prepared.restype = ctypes.c_int
     lib.kd_topk_kl_fwd_bwd_noalloc.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, i64, i64, i64,
                                                i32, f32, i64, vp, vp, vp, vp, vp]
     lib.kd_topk_kl_fwd_bwd_noalloc.restype = ctypes.c_int
@@ -386,32 +396,117 @@ def kd_timing_collect():
             for i in range(min(n.value, 32))}
 
 
-def dp_combine(loss, grad_h, grad_W, n_valid: int, group=None):
-    """Token-sharded data parallelism: each rank ran kd_topk_kl_fwd_bwd on its
-    own tokens, so its loss is the mean over its N_valid,r valid tokens and its
-    gradients carry 1/(T N_valid,r).  The loss of the whole batch is the mean
-    over all valid tokens, so every rank's results are reweighted by
-    N_valid,r / sum_r N_valid,r; then loss and grad_W are summed across ranks
-    (grad_h rows stay with their rank).  This is the one exchange the sharded
-    loss needs; grad_W's sum is the data-parallel gradient reduction a training
-    loop performs anyway.
-
-    loss [1] fp32, grad_h [N_r, d] fp32, grad_W [V, d] fp32 (updated in place);
-    n_valid: this rank's valid-token count.  Returns (loss, grad_h, grad_W)."""
+def kd_topk_kl_prepare(topk_idx, topk_logit, mask, N: int, d: int, V: int, T: float = 1.0,
+                       chunk: int = 0, dtype: int = KD_BF16, workspace=None, n_valid=None,
+                       err_flags=None, stream=None):
+    """Teacher preparation and the valid-row count of this rank's tokens, the
+    first half of a data-parallel step (see include/kd_topk_kl.h).  Returns
+    (n_valid [1] int64 on the device, workspace)."""
     import torch
-    import torch.distributed as dist
-    dev = grad_W.device
-    nv = torch.tensor([float(n_valid)], dtype=torch.float64, device=dev)
-    dist.all_reduce(nv, group=group)
-    total = float(nv.item())
-    w = float(n_valid) / total if total > 0 else 0.0
-    lw = (loss.to(torch.float64) * w).to(dev)
-    dist.all_reduce(lw, group=group)
-    loss.copy_(lw.to(loss.dtype))
-    grad_h.mul_(w)
-    grad_W.mul_(w)
-    dist.all_reduce(grad_W, group=group)
+    for name, t in (("topk_idx", topk_idx), ("topk_logit", topk_logit)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if topk_idx.dtype != torch.int32 or topk_logit.dtype != torch.float32:
+        raise TypeError("topk_idx must be int32 and topk_logit float32")
+    if topk_idx.shape != topk_logit.shape or topk_idx.shape[0] != N:
+        raise ValueError("shape mismatch")
+    if mask is not None and (mask.dtype != torch.uint8 or not mask.is_cuda
+                             or not mask.is_contiguous() or mask.shape != (N,)):
+        raise TypeError("mask must be a contiguous uint8 CUDA tensor of shape [N]")
+    K = topk_idx.shape[1]
+    dev = topk_idx.device
+    if workspace is None:
+        workspace = allocate_workspace(N, d, V, K, chunk, dtype, dev)
+    if n_valid is None:
+        n_valid = torch.empty(1, dtype=torch.int64, device=dev)
+    st = load_library().kd_topk_kl_prepare(
+        _ptr(topk_idx), _ptr(topk_logit), _ptr(mask), N, d, V, K, float(T), int(chunk), dtype,
+        _ptr(workspace), workspace.numel(), _ptr(n_valid), _ptr(err_flags), _stream_handle(stream))
+    _check(st, "kd_topk_kl_prepare")
+    return n_valid, workspace
+
+
+def kd_topk_kl_fwd_bwd_prepared(h, W, K: int, workspace, n_norm=None, T: float = 1.0,
+                                chunk: int = 0, loss=None, grad_h=None, grad_W=None,
+                                err_flags=None, stream=None):
+    """The chunk loop over a workspace that kd_topk_kl_prepare filled, with the
+    loss divided by n_norm ([1] int64 on the device; None: this rank's own
+    count).  Returns (loss, grad_h, grad_W)."""
+    import torch
+    for name, t in (("h", h), ("W", W)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if h.dtype != W.dtype:
+        raise TypeError("h and W must have the same dtype")
+    if n_norm is not None and (n_norm.dtype != torch.int64 or n_norm.device != h.device):
+        raise TypeError("n_norm must be an int64 tensor on h's device")
+    N, d = h.shape
+    V = W.shape[0]
+    dt = _dtype_code(h)
+    dev = h.device
+    if loss is None:
+        loss = torch.empty(1, dtype=torch.float32, device=dev)
+    if grad_h is None:
+        grad_h = torch.empty((N, d), dtype=torch.float32, device=dev)
+    if grad_W is None:
+        grad_W = torch.empty((V, d), dtype=torch.float32, device=dev)
+    st = load_library().kd_topk_kl_fwd_bwd_prepared(
+        _ptr(h), _ptr(W), dt, N, d, V, int(K), float(T), int(chunk), _ptr(n_norm), _ptr(loss),
+        _ptr(grad_h), _ptr(grad_W), _ptr(workspace), workspace.numel(), _ptr(err_flags),
+        _stream_handle(stream))
+    _check(st, "kd_topk_kl_fwd_bwd_prepared")
     return loss, grad_h, grad_W
+
+
+def kd_topk_kl_fwd_prepared(h, W, K: int, workspace, n_norm=None, T: float = 1.0,
+                            chunk: int = 0, loss=None, err_flags=None, stream=None):
+    """The loss alone over a prepared workspace, divided by n_norm.  Returns loss."""
+    import torch
+    if h.dtype != W.dtype:
+        raise TypeError("h and W must have the same dtype")
+    N, d = h.shape
+    V = W.shape[0]
+    if loss is None:
+        loss = torch.empty(1, dtype=torch.float32, device=h.device)
+    st = load_library().kd_topk_kl_fwd_prepared(
+        _ptr(h), _ptr(W), _dtype_code(h), N, d, V, int(K), float(T), int(chunk), _ptr(n_norm),
+        _ptr(loss), _ptr(workspace), workspace.numel(), _ptr(err_flags), _stream_handle(stream))
+    _check(st, "kd_topk_kl_fwd_prepared")
+    return loss
+
+
+def fwd_bwd_dp(h, W, topk_idx, topk_logit, mask=None, T: float = 1.0, chunk: int = 0,
+               group=None, loss=None, grad_h=None, grad_W=None, workspace=None, err_flags=None,
+               stream=None):
+    """One data-parallel step of the loss over this rank's token shard.
+
+    The batch's loss is the mean over all its valid tokens, so every rank
+    divides by the batch's N_valid: prepare this shard (its count on the
+    device), all-reduce the count, run the chunk loop with that divisor, then
+    all-reduce loss and grad_W (the reduction a data-parallel training loop
+    performs on its gradients anyway).  Every collective runs on the current
+    stream; nothing waits on the host.  grad_h rows stay with their rank.
+    With one rank (or torch.distributed not initialised) no collective runs
+    and the result equals kd_topk_kl_fwd_bwd.
+
+    Returns (loss [1], grad_h [N_r, d], grad_W [V, d], n_valid_total [1] int64,
+    workspace)."""
+    import torch.distributed as dist
+    N, d, V, K = _validate(h, W, topk_idx, topk_logit, mask)
+    dt = _dtype_code(h)
+    world = dist.get_world_size(group) if dist.is_available() and dist.is_initialized() else 1
+    n_valid, workspace = kd_topk_kl_prepare(topk_idx, topk_logit, mask, N, d, V, T, chunk, dt,
+                                            workspace=workspace, err_flags=err_flags,
+                                            stream=stream)
+    if world > 1:
+        dist.all_reduce(n_valid, group=group)
+    loss, grad_h, grad_W = kd_topk_kl_fwd_bwd_prepared(
+        h, W, K, workspace, n_norm=n_valid, T=T, chunk=chunk, loss=loss, grad_h=grad_h,
+        grad_W=grad_W, err_flags=err_flags, stream=stream)
+    if world > 1:
+        dist.all_reduce(grad_W, group=group)
+        dist.all_reduce(loss, group=group)
+    return loss, grad_h, grad_W, n_valid, workspace
 
 
 def status_string(st: int) -> str:
@@ -432,6 +527,9 @@ def workspace_view(workspace, lay: WorkspaceLayout, name: str, count: int, dtype
 fwd_bwd = kd_topk_kl_fwd_bwd
 fwd = kd_topk_kl_fwd
 fwd_bwd_noalloc = kd_topk_kl_fwd_bwd_noalloc
+prepare = kd_topk_kl_prepare
+fwd_bwd_prepared = kd_topk_kl_fwd_bwd_prepared
+fwd_prepared = kd_topk_kl_fwd_prepared
 topk_cache_build = kd_topk_cache_build
 full_kl_fwd_bwd = kd_full_kl_fwd_bwd
 timing_enable = kd_timing_enable

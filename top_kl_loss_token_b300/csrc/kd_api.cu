@@ -46,18 +46,28 @@ const char* const kKindNames[kNumKinds] = {
     "topk_candidates", "topk_select", "mask_rows", "full_pass1_gemm", "full_lse_combine",
     "full_grad_tile", "topk_refine", "topk_redo"};
 
+// Timing records and spare events.  An event belongs to the device that was
+// current when it was created and can be recorded only on that device's
+// streams, so the spare events are kept per device; one mutex guards all of
+// this state, so calls from several host threads may record concurrently.
 struct TimingRec {
   int kind;
+  int dev;
   cudaEvent_t a, b;
 };
+std::mutex g_timing_mu;
 bool g_timing_on = false;
 std::vector<TimingRec> g_recs;
-std::vector<cudaEvent_t> g_event_pool;
+std::vector<std::vector<cudaEvent_t>> g_event_pool;  // [device] spare events
 
-cudaEvent_t pooled_event() {
-  if (!g_event_pool.empty()) {
-    cudaEvent_t e = g_event_pool.back();
-    g_event_pool.pop_back();
+// A spare event of device `dev` (created there when none is left); the
+// caller holds g_timing_mu and `dev` is current.
+cudaEvent_t pooled_event(int dev) {
+  if (static_cast<int>(g_event_pool.size()) <= dev) g_event_pool.resize(dev + 1);
+  std::vector<cudaEvent_t>& pool = g_event_pool[dev];
+  if (!pool.empty()) {
+    cudaEvent_t e = pool.back();
+    pool.pop_back();
     return e;
   }
   cudaEvent_t e = nullptr;
@@ -68,18 +78,22 @@ cudaEvent_t pooled_event() {
 }  // namespace
 
 TimedLaunch::TimedLaunch(int k, cudaStream_t st) : kind(k), s(st) {
-  if (g_timing_on) {
-    a = pooled_event();
-    if (a != nullptr) cudaEventRecord(a, s);
-  }
+  std::lock_guard<std::mutex> lock(g_timing_mu);
+  if (!g_timing_on || cudaGetDevice(&dev) != cudaSuccess) return;
+  a = pooled_event(dev);
+  if (a != nullptr) cudaEventRecord(a, s);
 }
 
 TimedLaunch::~TimedLaunch() {
   if (a == nullptr) return;
-  cudaEvent_t b = pooled_event();
-  if (b == nullptr) return;
+  std::lock_guard<std::mutex> lock(g_timing_mu);
+  cudaEvent_t b = pooled_event(dev);
+  if (b == nullptr) {
+    g_event_pool[dev].push_back(a);
+    return;
+  }
   cudaEventRecord(b, s);
-  g_recs.push_back(TimingRec{kind, a, b});
+  g_recs.push_back(TimingRec{kind, dev, a, b});
 }
 
 bool encode_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
@@ -293,33 +307,46 @@ Views views(const Plan& P, void* ws) {
   return v;
 }
 
-kd_status run(const void* h, const void* W, kd_dtype dtype, const int32_t* topk_idx,
-              const float* topk_logit, const uint8_t* mask, int64_t N, int64_t d, int64_t V,
-              int32_t K, float T, int64_t chunk, float* loss, float* grad_h, float* grad_W,
-              bool want_grads, void* workspace, size_t ws_bytes, uint32_t* dev_err_flags,
-              cudaStream_t stream) {
-  const NvtxRange range(want_grads ? "kd_topk_kl_fwd_bwd" : "kd_topk_kl_fwd");
-  Plan P;
-  kd_status st = make_plan(N, d, V, K, chunk, dtype, &P);
+// Host-side checks of the sizes, the workspace and the stream's device; fills
+// the plan.  `need_grads`: the workspace must hold the exponential tile.
+kd_status check_call(int64_t N, int64_t d, int64_t V, int32_t K, float T, int64_t chunk,
+                     kd_dtype dtype, bool need_grads, const void* workspace, size_t ws_bytes,
+                     Plan* P) {
+  kd_status st = make_plan(N, d, V, K, chunk, dtype, P);
   if (st != KD_OK) return st;
   if (!(T > 0.f) || !isfinite(T)) return KD_ERR_INVALID_ARG;
-  if (W == nullptr || loss == nullptr) return KD_ERR_INVALID_ARG;
-  if (want_grads && grad_W == nullptr) return KD_ERR_INVALID_ARG;
-  if (N > 0 && (h == nullptr || topk_idx == nullptr || topk_logit == nullptr))
-    return KD_ERR_INVALID_ARG;
-  if (want_grads && N > 0 && grad_h == nullptr) return KD_ERR_INVALID_ARG;
-  if (!aligned16(W) || (N > 0 && !aligned16(h))) return KD_ERR_INVALID_ARG;
   // the loss alone never touches the last region (the chunk's exponential tile)
-  const size_t need = want_grads ? P.lay.total : P.lay.off_g;
+  const size_t need = need_grads ? P->lay.total : P->lay.off_g;
   if (workspace == nullptr || ws_bytes < need) return KD_ERR_WORKSPACE;
   if (!aligned16(workspace)) return KD_ERR_WORKSPACE;
-  const int sms = num_sms();
-  if (sms <= 0) return KD_ERR_CUDA;
-  if (dtype == KD_BF16 && encode_fn() == nullptr) return KD_ERR_CUDA;
+  return KD_OK;
+}
 
-  const Views v = views(P, workspace);
-  uint32_t* err = dev_err_flags != nullptr ? dev_err_flags : &v.ctrl->err;
+// Teacher preparation and the valid-row map: the per-call part of the loss
+// that does not touch h or W.  Clears the control words first.
+kd_status prepare(const int32_t* topk_idx, const float* topk_logit, const uint8_t* mask,
+                  const Plan& P, float T, const Views& v, int64_t* n_valid_out, uint32_t* err,
+                  cudaStream_t stream) {
   KD_CUDA(cudaMemsetAsync(v.ctrl, 0, sizeof(Ctrl), stream));
+  if (P.N == 0) {
+    if (n_valid_out != nullptr) KD_CUDA(cudaMemsetAsync(n_valid_out, 0, sizeof(int64_t), stream));
+    return KD_OK;
+  }
+  KD_LAUNCH(kTeacherPrep, launch_teacher_prep(topk_idx, topk_logit, mask, P.N, static_cast<int>(P.K),
+                                              P.V, T, v.row_ok, v.idx_sorted, v.p_sorted, v.plogp,
+                                              v.psum, err, stream));
+  KD_LAUNCH(kCompact, launch_compact(v.row_ok, P.N, v.rows, v.ctrl, n_valid_out, stream));
+  return KD_OK;
+}
+
+// The chunk loop over a prepared workspace: logsumexp pass, loss terms and,
+// with want_grads, the gradient tile and both gradient products per chunk;
+// then the loss.  Terms are divided by *n_norm.
+kd_status chunks(const void* h, const void* W, const Plan& P, float T, float* loss,
+                 float* grad_h, float* grad_W, bool want_grads, const Views& v,
+                 const int64_t* n_norm, uint32_t* err, int sms, cudaStream_t stream) {
+  const int64_t N = P.N, d = P.d, V = P.V;
+  const kd_dtype dtype = P.dtype;
   if (N == 0) {
     KD_CUDA(cudaMemsetAsync(loss, 0, sizeof(float), stream));
     if (want_grads)
@@ -327,10 +354,6 @@ kd_status run(const void* h, const void* W, kd_dtype dtype, const int32_t* topk_
     return KD_OK;
   }
   const float k2 = 1.4426950408889634f / T;
-
-  KD_LAUNCH(kTeacherPrep, launch_teacher_prep(topk_idx, topk_logit, mask, N, K, V, T, v.row_ok, v.idx_sorted,
-                              v.p_sorted, v.plogp, v.psum, err, stream));
-  KD_LAUNCH(kCompact, launch_compact(v.row_ok, N, v.rows, v.ctrl, stream));
   if (want_grads) KD_LAUNCH(kZeroRows, launch_zero_invalid_rows(v.row_ok, N, d, grad_h, stream));
 
   for (int64_t j = 0; j < P.n_chunks; ++j) {
@@ -340,10 +363,11 @@ kd_status run(const void* h, const void* W, kd_dtype dtype, const int32_t* topk_
     a.chunk = static_cast<int>(P.chunk);
     a.cpad = P.cpad;
     a.n_valid = &v.ctrl->n_valid;
+    a.n_norm = n_norm;
     a.rows = v.rows;
     a.idx_sorted = v.idx_sorted;
     a.p_sorted = v.p_sorted;
-    a.K = K;
+    a.K = static_cast<int>(P.K);
     a.V = static_cast<int>(V);
     a.n_pb = static_cast<int>(P.n_pb);
     a.ldg = P.ldg;
@@ -418,8 +442,62 @@ kd_status run(const void* h, const void* W, kd_dtype dtype, const int32_t* topk_
       KD_LAUNCH(kSimtGemm, launch_simt_gemm(gw, stream));
     }
   }
-  KD_LAUNCH(kFinalize, launch_finalize(v.loss_rows, v.ctrl, loss, stream));
+  KD_LAUNCH(kFinalize, launch_finalize(v.loss_rows, v.ctrl, n_norm, loss, stream));
   return KD_OK;
+}
+
+// Pointer checks of the chunk loop's arguments.
+kd_status check_outputs(const Plan& P, const void* h, const void* W, float* loss, float* grad_h,
+                        float* grad_W, bool want_grads) {
+  if (W == nullptr || loss == nullptr) return KD_ERR_INVALID_ARG;
+  if (want_grads && grad_W == nullptr) return KD_ERR_INVALID_ARG;
+  if (P.N > 0 && h == nullptr) return KD_ERR_INVALID_ARG;
+  if (want_grads && P.N > 0 && grad_h == nullptr) return KD_ERR_INVALID_ARG;
+  if (!aligned16(W) || (P.N > 0 && !aligned16(h))) return KD_ERR_INVALID_ARG;
+  return KD_OK;
+}
+
+kd_status run(const void* h, const void* W, kd_dtype dtype, const int32_t* topk_idx,
+              const float* topk_logit, const uint8_t* mask, int64_t N, int64_t d, int64_t V,
+              int32_t K, float T, int64_t chunk, float* loss, float* grad_h, float* grad_W,
+              bool want_grads, void* workspace, size_t ws_bytes, uint32_t* dev_err_flags,
+              cudaStream_t stream) {
+  const NvtxRange range(want_grads ? "kd_topk_kl_fwd_bwd" : "kd_topk_kl_fwd");
+  Plan P;
+  kd_status st = check_call(N, d, V, K, T, chunk, dtype, want_grads, workspace, ws_bytes, &P);
+  if (st != KD_OK) return st;
+  st = check_outputs(P, h, W, loss, grad_h, grad_W, want_grads);
+  if (st != KD_OK) return st;
+  if (N > 0 && (topk_idx == nullptr || topk_logit == nullptr)) return KD_ERR_INVALID_ARG;
+  const int sms = num_sms();
+  if (sms <= 0) return KD_ERR_CUDA;
+  if (dtype == KD_BF16 && encode_fn() == nullptr) return KD_ERR_CUDA;
+  const Views v = views(P, workspace);
+  uint32_t* err = dev_err_flags != nullptr ? dev_err_flags : &v.ctrl->err;
+  st = prepare(topk_idx, topk_logit, mask, P, T, v, nullptr, err, stream);
+  if (st != KD_OK) return st;
+  return chunks(h, W, P, T, loss, grad_h, grad_W, want_grads, v, &v.ctrl->n_valid64, err, sms,
+                stream);
+}
+
+kd_status run_prepared(const void* h, const void* W, kd_dtype dtype, int64_t N, int64_t d,
+                       int64_t V, int32_t K, float T, int64_t chunk, const int64_t* n_norm,
+                       float* loss, float* grad_h, float* grad_W, bool want_grads,
+                       void* workspace, size_t ws_bytes, uint32_t* dev_err_flags,
+                       cudaStream_t stream) {
+  const NvtxRange range(want_grads ? "kd_topk_kl_fwd_bwd_prepared" : "kd_topk_kl_fwd_prepared");
+  Plan P;
+  kd_status st = check_call(N, d, V, K, T, chunk, dtype, want_grads, workspace, ws_bytes, &P);
+  if (st != KD_OK) return st;
+  st = check_outputs(P, h, W, loss, grad_h, grad_W, want_grads);
+  if (st != KD_OK) return st;
+  const int sms = num_sms();
+  if (sms <= 0) return KD_ERR_CUDA;
+  if (dtype == KD_BF16 && encode_fn() == nullptr) return KD_ERR_CUDA;
+  const Views v = views(P, workspace);
+  uint32_t* err = dev_err_flags != nullptr ? dev_err_flags : &v.ctrl->err;
+  return chunks(h, W, P, T, loss, grad_h, grad_W, want_grads, v,
+                n_norm != nullptr ? n_norm : &v.ctrl->n_valid64, err, sms, stream);
 }
 
 }  // namespace
@@ -472,6 +550,38 @@ kd_status kd_topk_kl_fwd(const void* h, const void* W, kd_dtype dtype, const int
                          cudaStream_t stream) {
   return kd::run(h, W, dtype, topk_idx, topk_logit, mask, N, d, V, K, T, chunk, loss, nullptr,
                  nullptr, false, workspace, ws_bytes, dev_err_flags, stream);
+}
+
+kd_status kd_topk_kl_prepare(const int32_t* topk_idx, const float* topk_logit, const uint8_t* mask,
+                             int64_t N, int64_t d, int64_t V, int32_t K, float T, int64_t chunk,
+                             kd_dtype dtype, void* workspace, size_t ws_bytes, int64_t* n_valid,
+                             uint32_t* dev_err_flags, cudaStream_t stream) {
+  const kd::NvtxRange range("kd_topk_kl_prepare");
+  kd::Plan P;
+  // a loss-only workspace is enough here; the chunk loop checks its own need
+  kd_status st = kd::check_call(N, d, V, K, T, chunk, dtype, false, workspace, ws_bytes, &P);
+  if (st != KD_OK) return st;
+  if (N > 0 && (topk_idx == nullptr || topk_logit == nullptr)) return KD_ERR_INVALID_ARG;
+  const kd::Views v = kd::views(P, workspace);
+  uint32_t* err = dev_err_flags != nullptr ? dev_err_flags : &v.ctrl->err;
+  return kd::prepare(topk_idx, topk_logit, mask, P, T, v, n_valid, err, stream);
+}
+
+kd_status kd_topk_kl_fwd_bwd_prepared(const void* h, const void* W, kd_dtype dtype, int64_t N,
+                                      int64_t d, int64_t V, int32_t K, float T, int64_t chunk,
+                                      const int64_t* n_norm, float* loss, float* grad_h,
+                                      float* grad_W, void* workspace, size_t ws_bytes,
+                                      uint32_t* dev_err_flags, cudaStream_t stream) {
+  return kd::run_prepared(h, W, dtype, N, d, V, K, T, chunk, n_norm, loss, grad_h, grad_W, true,
+                          workspace, ws_bytes, dev_err_flags, stream);
+}
+
+kd_status kd_topk_kl_fwd_prepared(const void* h, const void* W, kd_dtype dtype, int64_t N,
+                                  int64_t d, int64_t V, int32_t K, float T, int64_t chunk,
+                                  const int64_t* n_norm, float* loss, void* workspace,
+                                  size_t ws_bytes, uint32_t* dev_err_flags, cudaStream_t stream) {
+  return kd::run_prepared(h, W, dtype, N, d, V, K, T, chunk, n_norm, loss, nullptr, nullptr, false,
+                          workspace, ws_bytes, dev_err_flags, stream);
 }
 
 kd_status kd_umma_gemm_bf16(const void* A, const void* B, float* D, int64_t M, int64_t N,
@@ -558,6 +668,7 @@ kd_status kd_umma_gemm_bf16_wait_test(const void* A, const void* B, float* D, in
 }
 
 kd_status kd_timing_enable(int on) {
+  std::lock_guard<std::mutex> lock(kd::g_timing_mu);
   kd::g_timing_on = on != 0;
   return KD_OK;
 }
@@ -566,16 +677,25 @@ kd_status kd_timing_collect(kd_timing_entry* out, int32_t max_entries, int32_t* 
   int64_t launches[kd::kNumKinds] = {0};
   double ms[kd::kNumKinds] = {0.0};
   kd_status st = KD_OK;
-  for (const kd::TimingRec& r : kd::g_recs) {
+  std::vector<kd::TimingRec> recs;
+  {
+    std::lock_guard<std::mutex> lock(kd::g_timing_mu);
+    recs.swap(kd::g_recs);
+  }
+  for (const kd::TimingRec& r : recs) {
     float t = 0.f;
     if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess)
       st = KD_ERR_CUDA;
     launches[r.kind] += 1;
     ms[r.kind] += t;
-    kd::g_event_pool.push_back(r.a);
-    kd::g_event_pool.push_back(r.b);
   }
-  kd::g_recs.clear();
+  {
+    std::lock_guard<std::mutex> lock(kd::g_timing_mu);
+    for (const kd::TimingRec& r : recs) {
+      kd::g_event_pool[r.dev].push_back(r.a);
+      kd::g_event_pool[r.dev].push_back(r.b);
+    }
+  }
   int32_t n = 0;
   for (int k = 0; k < kd::kNumKinds; ++k) {
     if (launches[k] == 0) continue;

@@ -166,7 +166,7 @@ kd_status kd_full_kl_fwd_bwd(const void* h_s, const void* W_s, const void* h_t, 
     return KD_OK;
   }
   KD_LAUNCH(kd::kMaskRows, kd::launch_mask_rows(mask, N, row_ok, stream));
-  KD_LAUNCH(kd::kCompact, kd::launch_compact(row_ok, N, rows, ctrl, stream));
+  KD_LAUNCH(kd::kCompact, kd::launch_compact(row_ok, N, rows, ctrl, nullptr, stream));
   KD_LAUNCH(kd::kZeroRows, kd::launch_zero_invalid_rows(row_ok, N, d_s, grad_h, stream));
 
   for (int64_t j = 0; j < P.n_chunks; ++j) {
@@ -177,6 +177,7 @@ kd_status kd_full_kl_fwd_bwd(const void* h_s, const void* W_s, const void* h_t, 
     a.chunk = static_cast<int>(P.chunk);
     a.cpad = P.cpad;
     a.n_valid = &ctrl->n_valid;
+    a.n_norm = &ctrl->n_valid64;
     a.rows = rows;
     a.V = static_cast<int>(V);
     a.n_pb = static_cast<int>(P.n_pb);
@@ -211,7 +212,7 @@ kd_status kd_full_kl_fwd_bwd(const void* h_s, const void* W_s, const void* h_t, 
                                                       P.chunk, a, grad_h, grad_W, j > 0 ? 1 : 0,
                                                       sched + 1, err, sms, stream));
   }
-  KD_LAUNCH(kd::kFinalize, kd::launch_finalize(loss_rows, ctrl, loss, stream));
+  KD_LAUNCH(kd::kFinalize, kd::launch_finalize(loss_rows, ctrl, &ctrl->n_valid64, loss, stream));
   return KD_OK;
 }
 

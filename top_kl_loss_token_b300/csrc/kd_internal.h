@@ -92,11 +92,13 @@ enum KernelKind {
 };
 
 // Brackets one kernel launch with CUDA events on its stream while timing is
-// enabled (host-side state shared by all calls; not thread-safe).
+// enabled (process-wide record guarded by a mutex; events of the current
+// device).
 struct TimedLaunch {
   TimedLaunch(int kind, cudaStream_t s);
   ~TimedLaunch();
   int kind;
+  int dev = 0;
   cudaStream_t s;
   cudaEvent_t a = nullptr;
 };
@@ -116,9 +118,10 @@ int64_t default_chunk(int64_t N, int64_t d, int64_t V, kd_dtype dtype);
 
 // Control words at the start of the workspace.
 struct Ctrl {
-  uint32_t err;     // error flags when the caller passes none
-  int32_t n_valid;  // number of valid rows
-  double loss_sum;  // sum of the per-row loss terms
+  uint32_t err;       // error flags when the caller passes none
+  int32_t n_valid;    // number of valid rows
+  double loss_sum;    // sum of the per-row loss terms
+  int64_t n_valid64;  // the same count, the default normaliser of the loss
 };
 
 // Per-chunk pointers into the workspace that the row kernels use.
@@ -126,7 +129,9 @@ struct ChunkArgs {
   int64_t row0;          // first compacted row of this chunk
   int chunk;             // capacity of the chunk, in rows
   int64_t cpad;          // row stride of the per-chunk statistic arrays
-  const int32_t* n_valid;
+  const int32_t* n_valid;  // valid rows of this call (compacted row count)
+  const int64_t* n_norm;   // the loss's divisor: this call's count, or the
+                           // count of the whole data-parallel batch
   const int32_t* rows;   // compacted row -> original row
   const int32_t* idx_sorted;
   const float* p_sorted;
@@ -145,15 +150,19 @@ cudaError_t launch_teacher_prep(const int32_t* idx, const float* logit, const ui
                                 int64_t N, int K, int64_t V, float T, int32_t* row_ok,
                                 int32_t* idx_sorted, float* p_sorted, float* plogp, float* psum,
                                 uint32_t* err, cudaStream_t s);
+// Compacted valid-row map and the count (also copied to *n_valid_out, a
+// device int64, when that is non-null).
 cudaError_t launch_compact(const int32_t* row_ok, int64_t N, int32_t* rows, Ctrl* ctrl,
-                           cudaStream_t s);
+                           int64_t* n_valid_out, cudaStream_t s);
 cudaError_t launch_gather_rows(const void* h, size_t elem, int64_t d, const ChunkArgs& a,
                                void* hc, cudaStream_t s);
 cudaError_t launch_bucket_offsets(const ChunkArgs& a, cudaStream_t s);
 cudaError_t launch_lse(const ChunkArgs& a, const float* plogp, const float* psum, float T,
                        float* lse, float* loss_rows, cudaStream_t s);
 cudaError_t launch_grad_tile(const ChunkArgs& a, void* g, size_t elem, float T, cudaStream_t s);
-cudaError_t launch_finalize(const float* loss_rows, Ctrl* ctrl, float* loss, cudaStream_t s);
+// loss = (sum of the valid rows' loss terms) / *n_norm (0 when *n_norm <= 0).
+cudaError_t launch_finalize(const float* loss_rows, Ctrl* ctrl, const int64_t* n_norm,
+                            float* loss, cudaStream_t s);
 cudaError_t launch_zero_invalid_rows(const int32_t* row_ok, int64_t N, int64_t d, float* grad_h,
                                      cudaStream_t s);
 

@@ -27,6 +27,12 @@ __device__ __forceinline__ int chunk_count(const int32_t* n_valid, int64_t row0,
   return c < 0 ? 0 : (c > chunk ? chunk : static_cast<int>(c));
 }
 
+// 1 / (T n) for the loss's divisor n; 0 when n <= 0 (no valid token anywhere).
+__device__ __forceinline__ float grad_scale(const int64_t* n_norm, float T) {
+  const int64_t n = *n_norm;
+  return n > 0 ? 1.0f / (T * static_cast<float>(n)) : 0.f;
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -206,7 +212,8 @@ constexpr int kScanThreads = 1024;
 __global__ void __launch_bounds__(kScanThreads) compact_kernel(const int32_t* __restrict__ row_ok,
                                                               int64_t N,
                                                               int32_t* __restrict__ rows,
-                                                              Ctrl* ctrl) {
+                                                              Ctrl* ctrl,
+                                                              int64_t* __restrict__ n_valid_out) {
   __shared__ int warp_tot[kScanThreads / 32];
   __shared__ int carry;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -232,7 +239,9 @@ __global__ void __launch_bounds__(kScanThreads) compact_kernel(const int32_t* __
   }
   if (tid == 0) {
     ctrl->n_valid = carry;
+    ctrl->n_valid64 = carry;
     ctrl->loss_sum = 0.0;
+    if (n_valid_out != nullptr) *n_valid_out = carry;
   }
 }
 
@@ -343,7 +352,7 @@ __global__ void __launch_bounds__(kLseRows * kLseGroups) lse_kernel(
   __syncthreads();
   if (!live) return;
   const float lse2 = sLse[x];
-  const float scale = 1.0f / (T * static_cast<float>(*a.n_valid));
+  const float scale = grad_scale(a.n_norm, T);
   for (int pb = y; pb < a.n_pb; pb += kLseGroups) {
     const int64_t o = static_cast<int64_t>(pb) * a.cpad + i;
     a.part_m[o] = ex2_approx(a.part_m[o] - lse2) * scale;
@@ -419,7 +428,7 @@ __global__ void __launch_bounds__(kGThreads) grad_tile_kernel(ChunkArgs a, E* __
   const int64_t r = a.rows[a.row0 + i];
   const int32_t* lidx = a.idx_sorted + r * a.K;
   const float* lp = a.p_sorted + r * a.K;
-  const float scale = 1.0f / (T * static_cast<float>(*a.n_valid));
+  const float scale = grad_scale(a.n_norm, T);
   for (int64_t v0 = static_cast<int64_t>(threadIdx.x) * W; v0 < a.ldg; v0 += kGThreads * W) {
     float f[W];
     if (v0 >= a.V) {
@@ -524,7 +533,7 @@ __global__ void __launch_bounds__(kLseRows * kLseGroups) lse_dual_kernel(
   __syncthreads();
   if (!live) return;
   const float lse2_t = sLseT[x], lse2_s = sLseS[x];
-  const float scale = 1.0f / (T * static_cast<float>(*a.n_valid));
+  const float scale = grad_scale(a.n_norm, T);
   for (int pb = y; pb < a.n_pb; pb += kLseGroups) {
     const int64_t o = static_cast<int64_t>(pb) * a.cpad + i;
     a.part_m[o] = ex2_approx(a.part_m[o] - lse2_s) * scale;
@@ -578,13 +587,17 @@ __global__ void __launch_bounds__(kGThreads) grad_tile_dual_kernel(
   }
 }
 
-// loss = (sum of the per-row terms, in fixed order, in fp64) / N_valid.
+// loss = (sum of the per-row terms, in fixed order, in fp64) / n_norm, where
+// n_norm is this call's N_valid or that of the whole data-parallel batch.
 constexpr int kFinThreads = 1024;
 
 __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const float* __restrict__ loss_rows,
-                                                              Ctrl* ctrl, float* loss) {
+                                                              Ctrl* ctrl,
+                                                              const int64_t* __restrict__ n_norm,
+                                                              float* loss) {
   __shared__ double sd[kFinThreads];
   const int nv = ctrl->n_valid;
+  const int64_t nn = *n_norm;
   double s = 0.0;
   for (int i = threadIdx.x; i < nv; i += kFinThreads) s += static_cast<double>(loss_rows[i]);
   sd[threadIdx.x] = s;
@@ -595,7 +608,7 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const float* __re
   }
   if (threadIdx.x == 0) {
     ctrl->loss_sum = sd[0];
-    *loss = nv > 0 ? static_cast<float>(sd[0] / static_cast<double>(nv)) : 0.f;
+    *loss = nn > 0 ? static_cast<float>(sd[0] / static_cast<double>(nn)) : 0.f;
   }
 }
 
@@ -792,8 +805,8 @@ cudaError_t launch_teacher_prep(const int32_t* idx, const float* logit, const ui
 }
 
 cudaError_t launch_compact(const int32_t* row_ok, int64_t N, int32_t* rows, Ctrl* ctrl,
-                           cudaStream_t s) {
-  compact_kernel<<<1, kScanThreads, 0, s>>>(row_ok, N, rows, ctrl);
+                           int64_t* n_valid_out, cudaStream_t s) {
+  compact_kernel<<<1, kScanThreads, 0, s>>>(row_ok, N, rows, ctrl, n_valid_out);
   return cudaGetLastError();
 }
 
@@ -840,8 +853,9 @@ cudaError_t launch_grad_tile(const ChunkArgs& a, void* g, size_t elem, float T, 
   return cudaGetLastError();
 }
 
-cudaError_t launch_finalize(const float* loss_rows, Ctrl* ctrl, float* loss, cudaStream_t s) {
-  finalize_kernel<<<1, kFinThreads, 0, s>>>(loss_rows, ctrl, loss);
+cudaError_t launch_finalize(const float* loss_rows, Ctrl* ctrl, const int64_t* n_norm,
+                            float* loss, cudaStream_t s) {
+  finalize_kernel<<<1, kFinThreads, 0, s>>>(loss_rows, ctrl, n_norm, loss);
   return cudaGetLastError();
 }
 
