@@ -40,17 +40,32 @@ extern "C" {
  *                             entries), 0 for the padding
  *   plogp:      fp32  [N]     sum of p ln p over row r's entries
  *   psum:       fp32  [N]     sum of p over row r's entries (1 up to rounding)
+ *   top1:       int32 [N]     index of row r's most probable entry (the lower
+ *                             index among equal probabilities)
  * The last chunk that holds valid rows, j = (N_valid - 1) / chunk, with
  * count = N_valid - j * chunk rows; its i-th row (i < count) is the original
  * row rows[j * chunk + i]:
  *   boff:       uint16 [n_pb + 1, chunk_pad]  boff[b][i] = position in that
  *                             row's sorted entries of the first one whose
  *                             index is >= 128 b
- *   g:          [chunk_pad, ld_g], bf16 (KD_BF16) or fp32 (KD_FP32), after
- *               kd_topk_kl_fwd_bwd only: the gradient of the loss with respect
- *               to the student logits, row i column v < V holding
- *               (softmax(s_i)_v - sum of p over the row's entries with index v)
- *               / (T N_valid) rounded to the type, columns V .. ld_g - 1 zero
+ *   g:          [chunk_pad, ld_g], after kd_topk_kl_fwd_bwd only: the
+ *               gradient of the loss with respect to the student logits,
+ *               dL/dz[i, v] = (softmax(s_i)_v - sum of p over the row's entries
+ *               with index v) / (T N_valid), for v < V:
+ *                 KD_FP32: dL/dz itself (fp32); columns V .. ld_g - 1 zero;
+ *                 KD_BF16: bf16 values g' with dL/dz[i, v] = alpha_i * g'[i, v]
+ *                          (alpha_i in rowstat below): the row's exponentials
+ *                          relative to one reference, minus the teacher's
+ *                          probabilities scaled to match
+ *   rowstat:    fp32 [4, N] (KD_BF16 with gradients), for the i-th valid row
+ *               of the call (every chunk, compacted order): [0] its reference
+ *               m_i (log2 units), [1] (int32) 1 if some vocabulary block kept
+ *               its own maximum as reference, [2] alpha_i, [3] 1 / (alpha_i T
+ *               N_valid); alpha_i of the last chunk's row i is at
+ *               [2, j * chunk + i]
+ *   hc:         [chunk_pad, d] the chunk's rows of h (KD_BF16 with gradients:
+ *               multiplied by alpha_i and rounded to bf16, so that grad_W
+ *               receives g'^T hc)
  * The other regions, and the rows of boff and g beyond count, are scratch
  * space whose contents are not specified.
  */
@@ -72,6 +87,8 @@ typedef struct {
   size_t off_part_l;
   size_t off_part_ps;
   size_t off_boff;
+  size_t off_top1;
+  size_t off_rowstat;
   size_t off_hc;
   size_t off_g;
   size_t off_sched;

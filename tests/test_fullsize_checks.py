@@ -1,7 +1,8 @@
 """The whole-matrix checks that the full-size GPU tests apply to grad_W and
 grad_h (tests/test_gpu_fullsize.py), run here on the CPU against the fp64
-oracle: they must pass on exact results and on results whose dL/dz tile
-carries the two bf16 roundings of the GPU path, and they must fail on planted
+oracle: they must pass on exact results and on results built the way the
+bf16 GPU path builds them (dL/dz = alpha g' with g' rounded to bf16, the
+gradient products taking g' and bf16(alpha h)), and they must fail on planted
 mistakes (the teacher term of dL/dz left out; one 256-row tile of grad_W, or
 one 128-row tile of grad_h, missing)."""
 import numpy as np
@@ -9,7 +10,7 @@ import pytest
 
 import oracle
 from top_kl_loss_token_b300 import synth
-from test_gpu_fullsize import check_projection_identity, check_sum_rule
+from test_gpu_fullsize import check_projection_identity, check_sum_rule, scaled_rows
 
 
 def _bf16(a):
@@ -39,6 +40,23 @@ def _outputs(x, G, n_valid):
     return dict(grad_W=G.T @ np.where(valid[:, None], h, 0.0), grad_h=G @ W, n_valid=n_valid)
 
 
+def _scaled_outputs(x, G, n_valid, seed=3):
+    """The bf16 path's products: per valid row a factor alpha (here random,
+    of the size 1 / (T N_valid) times a power-of-two spread), g' = bf16(G /
+    alpha), grad_h = alpha (g' W), grad_W = g'^T bf16(alpha h)."""
+    rng = np.random.default_rng(seed)
+    W = x.W_f32().astype(np.float64)
+    valid = np.ones(x.N, bool) if x.mask is None else x.mask != 0
+    rows = np.nonzero(valid)[0]
+    alpha = (2.0 ** rng.uniform(-6, 6, size=rows.size) / (x.T * n_valid)).astype(np.float32)
+    alpha = alpha.astype(np.float64)
+    gp = _bf16(G[rows] / alpha[:, None])
+    grad_h = np.zeros((x.N, x.d))
+    grad_h[rows] = alpha[:, None] * (gp @ W)
+    grad_W = gp.T @ scaled_rows(x, rows, alpha)
+    return dict(grad_W=grad_W, grad_h=grad_h, n_valid=n_valid, rows=rows), alpha
+
+
 def test_checks_pass_on_exact_and_on_rounded_results(problem):
     x, g, G, Gq = problem
     exact = _outputs(x, G, g["n_valid"])
@@ -47,6 +65,12 @@ def test_checks_pass_on_exact_and_on_rounded_results(problem):
     rounded = _outputs(x, Gq, g["n_valid"])
     assert check_sum_rule(x, rounded) <= 1.0
     check_projection_identity(x, rounded)
+    scaled, alpha = _scaled_outputs(x, Gq, g["n_valid"])
+    assert check_sum_rule(x, scaled) <= 1.0
+    assert check_projection_identity(x, scaled, alpha) < 1e-10
+    # without the factors the identity is off by the rounding of alpha h
+    with pytest.raises(AssertionError):
+        check_projection_identity(x, dict(scaled, grad_h=scaled["grad_h"] * 1.01), alpha)
 
 
 def test_sum_rule_catches_a_missing_teacher_term(problem):
@@ -61,16 +85,20 @@ def test_sum_rule_catches_a_missing_teacher_term(problem):
         check_sum_rule(x, _outputs(x, no_teacher, g["n_valid"]))
 
 
-def test_projection_identity_catches_a_missing_tile(problem):
+@pytest.mark.parametrize("scaled", [False, True])
+def test_projection_identity_catches_a_missing_tile(problem, scaled):
     x, g, G, Gq = problem
-    out = _outputs(x, Gq, g["n_valid"])
+    if scaled:
+        out, alpha = _scaled_outputs(x, Gq, g["n_valid"])
+    else:
+        out, alpha = _outputs(x, Gq, g["n_valid"]), None
     bad = dict(out)
     bad["grad_W"] = out["grad_W"].copy()
     bad["grad_W"][512:768] = 0.0
     with pytest.raises(AssertionError):
-        check_projection_identity(x, bad)
+        check_projection_identity(x, bad, alpha)
     bad = dict(out)
     bad["grad_h"] = out["grad_h"].copy()
     bad["grad_h"][1024:1152] = 0.0
     with pytest.raises(AssertionError):
-        check_projection_identity(x, bad)
+        check_projection_identity(x, bad, alpha)

@@ -56,6 +56,14 @@ def test_large_logits_do_not_overflow(kd):
     x.logit = (x.logit * 20).astype(np.float32)
     got, ref = _check(kd, x)
     assert np.isfinite(got["grad_W"]).all() and np.isfinite(got["loss"])
+    # The student's logits spread over hundreds of units, far above its logit
+    # at the teacher's most probable entry for most rows: those rows' blocks
+    # keep their own maxima in pass 1 and are brought to one reference before
+    # the gradient products (the row flag of the single chunk records it).
+    import torch
+    n = x.N
+    rs = kd.workspace_view(got["ws"], got["lay"], "rowstat", 4 * n, torch.int32).cpu().numpy()
+    assert rs[n: n + got["n_valid"]].sum() > got["n_valid"] // 2
 
 
 def test_one_token_one_word_vocabulary(kd):

@@ -36,6 +36,25 @@ def last_chunk(got, chunk, N):
     return j * c, got["n_valid"] - j * c
 
 
+def row_alpha(kd, got, N, row0, count):
+    """alpha_i of the chunk rows row0 .. row0 + count (bf16 with gradients)."""
+    import torch
+    rs = region(kd, got, "rowstat", 4 * N, torch.float32)
+    return rs[2 * N + row0: 2 * N + row0 + count].astype(np.float64)
+
+
+def stored_tile(kd, got, dtype, N, row0, count, cpad, ldg):
+    """The last chunk's dL/dz [count, ldg] as the workspace holds it: fp32
+    itself, or (bf16) the stored values times the row factor alpha_i."""
+    import torch
+    if dtype == "bf16":
+        g = region(kd, got, "g", cpad * ldg, torch.int16)
+        g = torch.from_numpy(g).view(torch.bfloat16).double().numpy().reshape(cpad, ldg)[:count]
+        return g * row_alpha(kd, got, N, row0, count)[:, None]
+    g = region(kd, got, "g", cpad * ldg, torch.float32).astype(np.float64).reshape(cpad, ldg)
+    return g[:count]
+
+
 def teacher_case():
     # duplicates, out-of-range indices and -inf logits in valid rows, plus masked rows
     x = synth.make_inputs(300, 64, 1100, 16, T=1.5, dtype="bf16", seed=201, mask="random0.2")
@@ -129,12 +148,7 @@ def test_gradient_tile(kd, dtype, chunk):
     lay = got["lay"]
     cpad, ldg = int(lay.chunk_pad), int(lay.ld_g)
     row0, count = last_chunk(got, chunk, x.N)
-    if dtype == "bf16":
-        g = region(kd, got, "g", cpad * ldg, torch.int16)
-        g = torch.from_numpy(g).view(torch.bfloat16).double().numpy()
-    else:
-        g = region(kd, got, "g", cpad * ldg, torch.float32).astype(np.float64)
-    g = g.reshape(cpad, ldg)
+    g = stored_tile(kd, got, dtype, x.N, row0, count, cpad, ldg)
     rows = got["rows"][row0:row0 + count]
     ref = oracle.grad_logits(x.h_f32(), x.W_f32(), x.idx, x.logit, x.mask, x.T)
     G_ref = ref["G"][rows]
@@ -166,17 +180,26 @@ def test_gradient_products_of_the_stored_tile(kd, dtype, chunk):
     lay = got["lay"]
     cpad, ldg = int(lay.chunk_pad), int(lay.ld_g)
     row0, count = last_chunk(got, chunk, x.N)
-    if dtype == "bf16":
-        g = region(kd, got, "g", cpad * ldg, torch.int16)
-        g = torch.from_numpy(g).view(torch.bfloat16).double().numpy()
-    else:
-        g = region(kd, got, "g", cpad * ldg, torch.float32).astype(np.float64)
-    G = g.reshape(cpad, ldg)[:count, :x.V]
     rows = got["rows"][row0:row0 + count]
     W = x.W_f32().astype(np.float64)
-    H = x.h_f32().astype(np.float64)[rows]
-    want_h = G @ W
-    bound_h = 3e-5 * (np.abs(G) @ np.abs(W)) + 1e-30
+    if dtype == "bf16":
+        # the stored operands of the products: g' (dL/dz = alpha g') and the
+        # chunk's h rows scaled by alpha (bf16): grad_h = alpha (g' W) and
+        # grad_W = g'^T (alpha h)
+        g = region(kd, got, "g", cpad * ldg, torch.int16)
+        G = torch.from_numpy(g).view(torch.bfloat16).double().numpy().reshape(cpad, ldg)
+        G = G[:count, :x.V]
+        alpha = row_alpha(kd, got, x.N, row0, count)[:, None]
+        hc = region(kd, got, "hc", cpad * x.d, torch.int16)
+        H = torch.from_numpy(hc).view(torch.bfloat16).double().numpy().reshape(cpad, x.d)
+        H = H[:count]
+    else:
+        g = region(kd, got, "g", cpad * ldg, torch.float32).astype(np.float64)
+        G = g.reshape(cpad, ldg)[:count, :x.V]
+        alpha = np.ones((count, 1))
+        H = x.h_f32().astype(np.float64)[rows]
+    want_h = alpha * (G @ W)
+    bound_h = 3e-5 * (np.abs(alpha * G) @ np.abs(W)) + 1e-30
     assert np.all(np.abs(got["grad_h"][rows] - want_h) <= bound_h)
     masked = np.setdiff1d(np.arange(x.N), got["rows"])
     assert np.all(got["grad_h"][masked] == 0.0)
@@ -184,3 +207,7 @@ def test_gradient_products_of_the_stored_tile(kd, dtype, chunk):
         want_W = G.T @ H
         bound_W = 3e-5 * (np.abs(G).T @ np.abs(H)) + 1e-30
         assert np.all(np.abs(got["grad_W"] - want_W) <= bound_W)
+        if dtype == "bf16":
+            # and the scaled rows are alpha h rounded once to bf16
+            h_ref = alpha * x.h_f32().astype(np.float64)[rows]
+            assert np.all(np.abs(H - h_ref) <= 2.0 ** -8 * np.abs(h_ref))

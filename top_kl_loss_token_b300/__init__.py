@@ -60,7 +60,7 @@ class WorkspaceLayout(ctypes.Structure):
         (n, ctypes.c_size_t) for n in (
             "off_ctrl", "off_row_ok", "off_rows", "off_idx_sorted", "off_p_sorted", "off_plogp",
             "off_psum", "off_lse", "off_loss_rows", "off_part_m", "off_part_l", "off_part_ps",
-            "off_boff", "off_hc", "off_g", "off_sched", "total")]
+            "off_boff", "off_top1", "off_rowstat", "off_hc", "off_g", "off_sched", "total")]
 
 
 class TimingEntry(ctypes.Structure):

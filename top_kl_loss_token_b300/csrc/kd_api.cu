@@ -44,7 +44,7 @@ const char* const kKindNames[kNumKinds] = {
     "pass1_gemm",   "lse_combine", "grad_tile",        "bwd_gemm",    "finalize",
     "simt_pass1",   "simt_gemm",   "topk_block_max",   "topk_threshold",
     "topk_candidates", "topk_select", "mask_rows", "full_pass1_gemm", "full_lse_combine",
-    "full_grad_tile", "topk_refine", "topk_redo"};
+    "full_grad_tile", "topk_refine", "topk_redo", "grad_prepare"};
 
 // Timing records and spare events.  An event belongs to the device that was
 // current when it was created and can be recorded only on that device's
@@ -190,6 +190,7 @@ kd_status make_plan(int64_t N, int64_t d, int64_t V, int32_t K, int64_t chunk, k
   L.off_rows = take(4 * n);
   L.off_idx_sorted = take(4 * nk);
   L.off_p_sorted = take(4 * nk);
+  L.off_top1 = take(4 * n);
   L.off_plogp = take(4 * n);
   L.off_psum = take(4 * n);
   L.off_lse = take(4 * n);
@@ -198,6 +199,7 @@ kd_status make_plan(int64_t N, int64_t d, int64_t V, int32_t K, int64_t chunk, k
   L.off_part_l = take(4 * part);
   L.off_part_ps = take(4 * part);
   L.off_boff = take(2 * (static_cast<size_t>(P.n_pb) + 1) * static_cast<size_t>(P.cpad));
+  L.off_rowstat = take(4 * 4 * n);
   L.off_hc = take(static_cast<size_t>(P.cpad) * static_cast<size_t>(d) * P.elem);
   L.off_sched = take(256);
   // last: the loss alone stops here (kd_topk_kl_fwd_workspace_bytes)
@@ -210,7 +212,7 @@ cudaError_t launch_backward_gemms(const void* G, const void* W, const void* hc, 
                                   int64_t V, int64_t cpad, int64_t ldg, int64_t chunk,
                                   const ChunkArgs& a, float* grad_h, float* grad_W,
                                   int accumulate, uint32_t* counter, uint32_t* err, int sms,
-                                  cudaStream_t stream) {
+                                  cudaStream_t stream, const float* grad_h_scale) {
   TcGemmArgs g;
   memset(&g, 0, sizeof(g));
   TcProblem& gh = g.pr[0];  // grad_h rows of the chunk = G_c W
@@ -231,6 +233,7 @@ cudaError_t launch_backward_gemms(const void* G, const void* W, const void* hc, 
   gh.ldo = d;
   gh.row_map = a.rows;
   gh.row_map_off = a.row0;
+  gh.row_scale = grad_h_scale;
   gh.accumulate = 0;
   gh.count_mode = 1;
   TcProblem& gw = g.pr[1];  // grad_W (+)= G_c^T h_c
@@ -279,6 +282,11 @@ struct Views {
   float* part_l;
   float* part_ps;
   uint16_t* boff;
+  int32_t* top1;
+  float* mref;
+  int32_t* row_flag;
+  float* alpha_row;
+  float* beta_row;
   void* hc;
   void* g;
   uint32_t* sched;
@@ -301,6 +309,12 @@ Views views(const Plan& P, void* ws) {
   v.part_l = reinterpret_cast<float*>(b + L.off_part_l);
   v.part_ps = reinterpret_cast<float*>(b + L.off_part_ps);
   v.boff = reinterpret_cast<uint16_t*>(b + L.off_boff);
+  v.top1 = reinterpret_cast<int32_t*>(b + L.off_top1);
+  float* rs = reinterpret_cast<float*>(b + L.off_rowstat);
+  v.mref = rs;
+  v.row_flag = reinterpret_cast<int32_t*>(rs + P.N);
+  v.alpha_row = rs + 2 * P.N;
+  v.beta_row = rs + 3 * P.N;
   v.hc = b + L.off_hc;
   v.g = b + L.off_g;
   v.sched = reinterpret_cast<uint32_t*>(b + L.off_sched);
@@ -334,7 +348,7 @@ kd_status prepare(const int32_t* topk_idx, const float* topk_logit, const uint8_
   }
   KD_LAUNCH(kTeacherPrep, launch_teacher_prep(topk_idx, topk_logit, mask, P.N, static_cast<int>(P.K),
                                               P.V, T, v.row_ok, v.idx_sorted, v.p_sorted, v.plogp,
-                                              v.psum, err, stream));
+                                              v.psum, v.top1, err, stream));
   KD_LAUNCH(kCompact, launch_compact(v.row_ok, P.N, v.rows, v.ctrl, n_valid_out, stream));
   return KD_OK;
 }
@@ -359,6 +373,7 @@ kd_status chunks(const void* h, const void* W, const Plan& P, float T, float* lo
   for (int64_t j = 0; j < P.n_chunks; ++j) {
     const NvtxRange chunk_range("chunk");
     ChunkArgs a;
+    memset(&a, 0, sizeof(a));
     a.row0 = j * P.chunk;
     a.chunk = static_cast<int>(P.chunk);
     a.cpad = P.cpad;
@@ -375,8 +390,18 @@ kd_status chunks(const void* h, const void* W, const Plan& P, float T, float* lo
     a.part_m = v.part_m;
     a.part_l = v.part_l;
     a.part_ps = v.part_ps;
+    // bf16 with gradients: one reference per row, so that the gradient
+    // products read the stored exponentials directly (no pass over the
+    // chunk's vocabulary-wide tile between the GEMMs)
+    // (the per-row values are kept for every valid row, in compacted order;
+    // the kernels index them from the chunk's first row)
+    const bool row_ref = dtype == KD_BF16 && want_grads;
+    a.mref = row_ref ? v.mref + a.row0 : nullptr;
+    a.row_flag = row_ref ? v.row_flag + a.row0 : nullptr;
+    a.alpha_row = row_ref ? v.alpha_row + a.row0 : nullptr;
+    a.beta_row = row_ref ? v.beta_row + a.row0 : nullptr;
 
-    KD_LAUNCH(kGatherRows, launch_gather_rows(h, P.elem, d, a, v.hc, stream));
+    KD_LAUNCH(kGatherRows, launch_gather_rows(h, P.elem, d, a, v.hc, W, v.top1, k2, stream));
     KD_LAUNCH(kBucketOffsets, launch_bucket_offsets(a, stream));
     if (dtype == KD_BF16) {
       Pass1Args p1;
@@ -384,6 +409,7 @@ kd_status chunks(const void* h, const void* W, const Plan& P, float T, float* lo
       p1.W = W;
       p1.d = d;
       p1.k2 = k2;
+      p1.row_ref = row_ref;
       // the loss alone needs no stored exponentials
       p1.u = want_grads ? static_cast<uint16_t*>(v.g) : nullptr;
       p1.counter = v.sched;
@@ -396,12 +422,14 @@ kd_status chunks(const void* h, const void* W, const Plan& P, float T, float* lo
     }
     KD_LAUNCH(kLseCombine, launch_lse(a, v.plogp, v.psum, T, v.lse, v.loss_rows, stream));
     if (!want_grads) continue;
-    KD_LAUNCH(kGradTile, launch_grad_tile(a, v.g, P.elem, T, stream));
     if (dtype == KD_BF16) {
+      KD_LAUNCH(kGradPrepare, launch_grad_prepare(a, static_cast<uint16_t*>(v.g),
+                                                  static_cast<uint16_t*>(v.hc), d, stream));
       KD_LAUNCH(kBwdGemm, launch_backward_gemms(v.g, W, v.hc, d, V, P.cpad, P.ldg, P.chunk, a,
                                                 grad_h, grad_W, j > 0 ? 1 : 0, v.sched + 1, err,
-                                                sms, stream));
+                                                sms, stream, a.alpha_row));
     } else {
+      KD_LAUNCH(kGradTile, launch_grad_tile(a, v.g, P.elem, T, stream));
       const float* G = static_cast<const float*>(v.g);
       SimtGemm gh;
       memset(&gh, 0, sizeof(gh));

@@ -185,8 +185,10 @@ kd_status kd_full_kl_fwd_bwd(const void* h_s, const void* W_s, const void* h_t, 
     a.part_m = part_m;
     a.part_l = part_l;
 
-    KD_LAUNCH(kd::kGatherRows, kd::launch_gather_rows(h_s, 2, d_s, a, hc_s, stream));
-    KD_LAUNCH(kd::kGatherRows, kd::launch_gather_rows(h_t, 2, d_t, a, hc_t, stream));
+    KD_LAUNCH(kd::kGatherRows,
+              kd::launch_gather_rows(h_s, 2, d_s, a, hc_s, nullptr, nullptr, 0.f, stream));
+    KD_LAUNCH(kd::kGatherRows,
+              kd::launch_gather_rows(h_t, 2, d_t, a, hc_t, nullptr, nullptr, 0.f, stream));
     kd::DualPass1Args p1;
     memset(&p1, 0, sizeof(p1));
     p1.hc_t = hc_t;

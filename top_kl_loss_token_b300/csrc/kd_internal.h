@@ -88,6 +88,7 @@ enum KernelKind {
   kFullGradTile,
   kTopkRefine,
   kTopkRedo,
+  kGradPrepare,
   kNumKinds
 };
 
@@ -140,26 +141,53 @@ struct ChunkArgs {
   int n_pb;
   int64_t ldg;
   uint16_t* boff;        // [n_pb + 1][cpad] first sorted entry of each 128-column block
-  float* part_m;         // [n_pb][cpad]  block max of z * log2(e) / T (then alpha)
-  float* part_l;         // [n_pb][cpad]  block sum of 2^(s2 - m2)
+  float* part_m;         // [n_pb][cpad]  reference of block b's exponentials (then alpha_b)
+  float* part_l;         // [n_pb][cpad]  block sum of 2^(s2 - reference)
   float* part_ps;        // [n_pb][cpad]  block sum of p_k * s2_k over teacher entries
+  // One reference per row (bf16 path with gradients; nullptr otherwise),
+  // indexed by the chunk's row i (the arrays start at the chunk's first row):
+  float* mref;           // row i's reference m_i (log2 units): the student's
+                         // logit at the teacher's most probable entry
+  int32_t* row_flag;     // 1: some block of row i kept its own maximum
+  float* alpha_row;      // 2^(M_i - lse2_i) / (T n): dL/dz = alpha_row * stored tile
+  float* beta_row;       // 2^(lse2_i - M_i)
 };
 
+// A block of pass 1 stores its exponentials relative to the row's reference
+// m_i when its own maximum is at most this far (log2 units) above m_i, so the
+// stored values stay below 2^kRefSlack and the gradient products' fp32 sums
+// far from overflow; otherwise relative to its own maximum (and the row is
+// rescaled to one reference before the gradient products).
+constexpr float kRefSlack = 40.f;
+
 // ----------------------------------------------------------- row kernels
+// top1 (optional, [N]): index of each valid row's most probable teacher entry.
 cudaError_t launch_teacher_prep(const int32_t* idx, const float* logit, const uint8_t* mask,
                                 int64_t N, int K, int64_t V, float T, int32_t* row_ok,
                                 int32_t* idx_sorted, float* p_sorted, float* plogp, float* psum,
-                                uint32_t* err, cudaStream_t s);
+                                int32_t* top1, uint32_t* err, cudaStream_t s);
 // Compacted valid-row map and the count (also copied to *n_valid_out, a
 // device int64, when that is non-null).
 cudaError_t launch_compact(const int32_t* row_ok, int64_t N, int32_t* rows, Ctrl* ctrl,
                            int64_t* n_valid_out, cudaStream_t s);
+// With a.mref != nullptr (bf16), also the row references m_i = k2 * h_r . W[top1_r]
+// and cleared row flags.
 cudaError_t launch_gather_rows(const void* h, size_t elem, int64_t d, const ChunkArgs& a,
-                               void* hc, cudaStream_t s);
+                               void* hc, const void* W, const int32_t* top1, float k2,
+                               cudaStream_t s);
 cudaError_t launch_bucket_offsets(const ChunkArgs& a, cudaStream_t s);
 cudaError_t launch_lse(const ChunkArgs& a, const float* plogp, const float* psum, float T,
                        float* lse, float* loss_rows, cudaStream_t s);
 cudaError_t launch_grad_tile(const ChunkArgs& a, void* g, size_t elem, float T, cudaStream_t s);
+// bf16 path with one reference per row: prepares the stored exponentials u
+// [cpad, ldg] and the gathered h [cpad, d] for the gradient products:
+//   rows whose blocks kept their own maximum are rescaled to one reference;
+//   u[i, v] -= (sum of p over row i's teacher entries at v) * beta_row[i];
+//   hc[i, :] = alpha_row[i] * hc[i, :]  (bf16);
+//   rows count .. round_up(count, 64) of u are zeroed.
+// Then dL/dz = alpha_row * u, grad_h = alpha_row * (u W), grad_W = u^T hc.
+cudaError_t launch_grad_prepare(const ChunkArgs& a, uint16_t* u, uint16_t* hc, int64_t d,
+                                cudaStream_t s);
 // loss = (sum of the valid rows' loss terms) / *n_norm (0 when *n_norm <= 0).
 cudaError_t launch_finalize(const float* loss_rows, Ctrl* ctrl, const int64_t* n_norm,
                             float* loss, cudaStream_t s);
@@ -215,6 +243,7 @@ struct Pass1Args {
   const void* W;   // [V, d] bf16
   int64_t d;
   float k2;        // log2(e) / T
+  bool row_ref;    // store u relative to the row references a.mref
   uint16_t* u;     // [cpad, ldg] bf16, written; nullptr: not stored (the loss alone)
   uint32_t* counter;
   uint32_t* err;
@@ -237,6 +266,7 @@ struct TcProblem {
   int64_t M, N, K;   // output rows, output columns, reduction length (capacities)
   float* out;
   int64_t ldo;
+  const float* row_scale;  // optional: output row m is multiplied by row_scale[m]
   const int32_t* row_map;  // output row = row_map[row_map_off + m] when non-null
   int64_t row_map_off;
   int accumulate;
@@ -259,13 +289,14 @@ struct TcGemmArgs {
 cudaError_t launch_tc_gemm(const TcGemmArgs& g, cudaStream_t s);
 
 // The backward of one chunk in one launch: grad_h rows of the chunk = G_c W
-// (stored through the compacted row map) and grad_W (+)= G_c^T h_c.
+// (stored through the compacted row map; row i multiplied by grad_h_scale[i]
+// when given) and grad_W (+)= G_c^T h_c.
 // G [cpad, ldg] bf16, W [V, d] bf16, hc [cpad, d] bf16.
 cudaError_t launch_backward_gemms(const void* G, const void* W, const void* hc, int64_t d,
                                   int64_t V, int64_t cpad, int64_t ldg, int64_t chunk,
                                   const ChunkArgs& a, float* grad_h, float* grad_W,
                                   int accumulate, uint32_t* counter, uint32_t* err, int sms,
-                                  cudaStream_t stream);
+                                  cudaStream_t stream, const float* grad_h_scale = nullptr);
 
 // Full-vocabulary loss, pass 1 over one chunk: teacher and student logits of
 // each tile (problems 0 and 1 of one launch), their per-block statistics and

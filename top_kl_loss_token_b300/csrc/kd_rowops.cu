@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(kPrepThreads) teacher_prep_kernel(
     const uint8_t* __restrict__ mask, int K, int64_t V, float k2, int P2,
     int32_t* __restrict__ row_ok, int32_t* __restrict__ idx_sorted,
     float* __restrict__ p_sorted, float* __restrict__ plogp, float* __restrict__ psum,
-    uint32_t* __restrict__ err) {
+    int32_t* __restrict__ top1, uint32_t* __restrict__ err) {
   extern __shared__ uint8_t sm[];
   int32_t* skey = reinterpret_cast<int32_t*>(sm);
   float* sval = reinterpret_cast<float*>(skey + P2);
@@ -146,10 +146,13 @@ __global__ void __launch_bounds__(kPrepThreads) teacher_prep_kernel(
   for (int w = 0; w < kPrepThreads / 32; ++w) sum += red_f[w];
   __syncthreads();
 
-  // Pass C: probabilities, sum p ln p, sum p.
+  // Pass C: probabilities, sum p ln p, sum p, and the most probable entry
+  // (the lower index among equal probabilities).
   const float inv = 1.0f / sum;
   const float lgsum = lg2_approx(sum);
   float pl = 0.f, ps = 0.f;
+  float pbest = -1.f;
+  int ibest = kNoIndex;
   for (int k = tid; k < P2; k += kPrepThreads) {
     const float e = sval[k];
     const float p = e * inv;
@@ -157,25 +160,49 @@ __global__ void __launch_bounds__(kPrepThreads) teacher_prep_kernel(
       // ln p = ln(e) - ln(sum) with ln(e) = log2(e) * ln 2
       pl += p * (lg2_approx(e) - lgsum) * kLn2;
     }
+    if (skey[k] != kNoIndex && (p > pbest || (p == pbest && skey[k] < ibest))) {
+      pbest = p;
+      ibest = skey[k];
+    }
     ps += p;
     sval[k] = p;
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float po = __shfl_xor_sync(0xffffffffu, pbest, o);
+    const int io = __shfl_xor_sync(0xffffffffu, ibest, o);
+    if (po > pbest || (po == pbest && io < ibest)) {
+      pbest = po;
+      ibest = io;
+    }
+  }
+  __shared__ float red_pb[kPrepThreads / 32];
+  __shared__ int red_ib[kPrepThreads / 32];
   pl = warp_sum(pl);
   ps = warp_sum(ps);
   if (lane == 0) {
     red_f[wid] = pl;
     red_i[wid] = __float_as_int(ps);
+    red_pb[wid] = pbest;
+    red_ib[wid] = ibest;
   }
   __syncthreads();
   if (tid == 0) {
     float a = 0.f, b = 0.f;
+    float pb = -1.f;
+    int ib = kNoIndex;
 #pragma unroll
     for (int w = 0; w < kPrepThreads / 32; ++w) {
       a += red_f[w];
       b += __int_as_float(red_i[w]);
+      if (red_pb[w] > pb || (red_pb[w] == pb && red_ib[w] < ib)) {
+        pb = red_pb[w];
+        ib = red_ib[w];
+      }
     }
     plogp[r] = a;
     psum[r] = b;
+    if (top1 != nullptr) top1[r] = ib;
   }
 
   // Bitonic sort of (key, p) by key over P2 (a power of two) slots.
@@ -249,8 +276,15 @@ __global__ void __launch_bounds__(kScanThreads) compact_kernel(const int32_t* __
 
 // hc[i, :] = h[rows[row0 + i], :] for the chunk's valid rows; zero rows up to
 // the next multiple of 128 so the tensor-core tiles never read stale data.
-__global__ void gather_rows_kernel(const uint8_t* __restrict__ h, int64_t row_bytes,
-                                   ChunkArgs a, uint8_t* __restrict__ hc) {
+// With a.mref (bf16 only): also row i's reference m_i = k2 * (h_r . W[top1_r]),
+// the student's logit at the teacher's most probable entry in log2 units (a
+// value the row's logits reach, so exponentials relative to it stay in
+// range), and a cleared row flag.
+constexpr int kGatherThreads = 128;
+
+__global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(
+    const uint8_t* __restrict__ h, int64_t row_bytes, ChunkArgs a, uint8_t* __restrict__ hc,
+    const uint8_t* __restrict__ W, const int32_t* __restrict__ top1, float k2) {
   const int i = blockIdx.x;
   const int count = chunk_count(a.n_valid, a.row0, a.chunk);
   if (i >= round_up(count, 128)) return;
@@ -259,9 +293,40 @@ __global__ void gather_rows_kernel(const uint8_t* __restrict__ h, int64_t row_by
   if (i < count) {
     const int64_t r = a.rows[a.row0 + i];
     const uint4* src = reinterpret_cast<const uint4*>(h + r * row_bytes);
-    for (int64_t j = threadIdx.x; j < n16; j += blockDim.x) dst[j] = src[j];
+    if (a.mref == nullptr) {
+      for (int64_t j = threadIdx.x; j < n16; j += blockDim.x) dst[j] = src[j];
+      return;
+    }
+    const uint4* wrow = reinterpret_cast<const uint4*>(W + static_cast<int64_t>(top1[r]) * row_bytes);
+    float dot = 0.f;
+    for (int64_t j = threadIdx.x; j < n16; j += blockDim.x) {
+      const uint4 x = src[j];
+      const uint4 w = __ldg(wrow + j);
+      dst[j] = x;
+      const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        dot = fmaf(bf16lo_to_f32(xs[q]), bf16lo_to_f32(ws[q]), dot);
+        dot = fmaf(bf16hi_to_f32(xs[q]), bf16hi_to_f32(ws[q]), dot);
+      }
+    }
+    __shared__ float red[kGatherThreads / 32];
+    dot = warp_sum(dot);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = dot;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float t = 0.f;
+#pragma unroll
+      for (int w = 0; w < kGatherThreads / 32; ++w) t += red[w];
+      a.mref[i] = t * k2;
+      a.row_flag[i] = 0;
+    }
   } else {
     for (int64_t j = threadIdx.x; j < n16; j += blockDim.x) dst[j] = make_uint4(0, 0, 0, 0);
+    if (a.mref != nullptr && threadIdx.x == 0) {
+      a.mref[i] = 0.f;
+      a.row_flag[i] = 0;
+    }
   }
 }
 
@@ -348,6 +413,13 @@ __global__ void __launch_bounds__(kLseRows * kLseGroups) lse_kernel(
     lse_out[a.row0 + i] = lse2 * kLn2;
     loss_rows[a.row0 + i] = loss;
     sLse[x] = lse2;
+    if (a.alpha_row != nullptr) {
+      // MM is the row's common reference: its own m_i, or, when some block
+      // kept its own maximum, the largest block reference (the row is then
+      // rescaled to it before the gradient products)
+      a.alpha_row[i] = ex2_approx(MM - lse2) * grad_scale(a.n_norm, T);
+      a.beta_row[i] = ex2_approx(lse2 - MM);
+    }
   }
   __syncthreads();
   if (!live) return;
@@ -452,6 +524,78 @@ __global__ void __launch_bounds__(kGThreads) grad_tile_kernel(ChunkArgs a, E* __
       }
     }
     GVec<E>::store(row + v0, f);
+  }
+}
+
+// Prepares one chunk's stored exponentials and gathered h for the gradient
+// products when every row has one reference (kd_internal.h,
+// launch_grad_prepare).  One block per row i < round_up(count, 64).
+constexpr int kPrepGradThreads = 128;
+
+__global__ void __launch_bounds__(kPrepGradThreads) grad_prepare_kernel(
+    ChunkArgs a, uint16_t* __restrict__ u, uint16_t* __restrict__ hc, int64_t d) {
+  const int i = blockIdx.x;
+  const int count = chunk_count(a.n_valid, a.row0, a.chunk);
+  if (i >= round_up(count, 64)) return;
+  uint16_t* row = u + static_cast<int64_t>(i) * a.ldg;
+  const int tid = threadIdx.x;
+  if (i >= count) {
+    // the grad_W product reads whole 64-row blocks: rows past count are zero
+    for (int64_t v0 = static_cast<int64_t>(tid) * 8; v0 < a.ldg; v0 += kPrepGradThreads * 8)
+      *reinterpret_cast<uint4*>(row + v0) = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
+  // columns past the last 128-column block, which pass 1 does not write
+  for (int64_t v0 = static_cast<int64_t>(a.n_pb) * kPB + tid * 8; v0 < a.ldg;
+       v0 += kPrepGradThreads * 8)
+    *reinterpret_cast<uint4*>(row + v0) = make_uint4(0u, 0u, 0u, 0u);
+  const float ar = a.alpha_row[i];
+  if (a.row_flag[i] != 0 && ar > 0.f) {
+    // Some blocks of this row kept their own maximum as reference: bring every
+    // block to the row's common reference M (alpha_b / alpha_row =
+    // 2^(ref_b - M), at most 1).
+    for (int pb = tid; pb < a.n_pb; pb += kPrepGradThreads) {
+      const float f = a.part_m[static_cast<int64_t>(pb) * a.cpad + i] / ar;
+      if (f == 1.0f) continue;
+      uint4* p4 = reinterpret_cast<uint4*>(row + static_cast<int64_t>(pb) * kPB);
+#pragma unroll 4
+      for (int q = 0; q < kPB / 8; ++q) {
+        const uint4 x = p4[q];
+        p4[q] = make_uint4(pack_bf16x2(bf16lo_to_f32(x.x) * f, bf16hi_to_f32(x.x) * f),
+                           pack_bf16x2(bf16lo_to_f32(x.y) * f, bf16hi_to_f32(x.y) * f),
+                           pack_bf16x2(bf16lo_to_f32(x.z) * f, bf16hi_to_f32(x.z) * f),
+                           pack_bf16x2(bf16lo_to_f32(x.w) * f, bf16hi_to_f32(x.w) * f));
+      }
+    }
+    __syncthreads();
+  }
+  if (tid < 32) {
+    // Teacher entries: u[i, v] -= p_v * beta_row, so that alpha_row * u becomes
+    // (softmax - p) / (T n).  The sorted list keeps equal indices together:
+    // each run is summed first and applied once, by the lane that owns its
+    // first entry (distinct runs touch distinct columns).
+    const float br = a.beta_row[i];
+    const int64_t r = a.rows[a.row0 + i];
+    const int32_t* lidx = a.idx_sorted + r * a.K;
+    const float* lp = a.p_sorted + r * a.K;
+    for (int e = tid; e < a.K; e += 32) {
+      const int v = __ldg(lidx + e);
+      if (v == kNoIndex || (e > 0 && __ldg(lidx + e - 1) == v)) continue;
+      float ps = __ldg(lp + e);
+      for (int f = e + 1; f < a.K && __ldg(lidx + f) == v; ++f) ps += __ldg(lp + f);
+      uint16_t* at = row + v;
+      const float x = __uint_as_float(static_cast<uint32_t>(*at) << 16);
+      *at = static_cast<uint16_t>(pack_bf16x2(fmaf(-ps, br, x), 0.f) & 0xFFFFu);
+    }
+  }
+  // h of this row scaled by alpha_row: grad_W = u^T (alpha_row h)
+  uint4* h4 = reinterpret_cast<uint4*>(hc + static_cast<int64_t>(i) * d);
+  for (int64_t j = tid; j < d / 8; j += kPrepGradThreads) {
+    const uint4 x = h4[j];
+    h4[j] = make_uint4(pack_bf16x2(bf16lo_to_f32(x.x) * ar, bf16hi_to_f32(x.x) * ar),
+                       pack_bf16x2(bf16lo_to_f32(x.y) * ar, bf16hi_to_f32(x.y) * ar),
+                       pack_bf16x2(bf16lo_to_f32(x.z) * ar, bf16hi_to_f32(x.z) * ar),
+                       pack_bf16x2(bf16lo_to_f32(x.w) * ar, bf16hi_to_f32(x.w) * ar));
   }
 }
 
@@ -791,7 +935,7 @@ int next_pow2(int x) {
 cudaError_t launch_teacher_prep(const int32_t* idx, const float* logit, const uint8_t* mask,
                                 int64_t N, int K, int64_t V, float T, int32_t* row_ok,
                                 int32_t* idx_sorted, float* p_sorted, float* plogp, float* psum,
-                                uint32_t* err, cudaStream_t s) {
+                                int32_t* top1, uint32_t* err, cudaStream_t s) {
   if (N == 0) return cudaSuccess;
   const int P2 = next_pow2(K < 2 ? 2 : K);
   const size_t smem = static_cast<size_t>(P2) * 8;
@@ -800,7 +944,8 @@ cudaError_t launch_teacher_prep(const int32_t* idx, const float* logit, const ui
                                        static_cast<int>(smem < 48 * 1024 ? 48 * 1024 : smem));
   if (e != cudaSuccess) return e;
   teacher_prep_kernel<<<static_cast<unsigned>(N), kPrepThreads, smem, s>>>(
-      idx, logit, mask, K, V, kLog2e / T, P2, row_ok, idx_sorted, p_sorted, plogp, psum, err);
+      idx, logit, mask, K, V, kLog2e / T, P2, row_ok, idx_sorted, p_sorted, plogp, psum, top1,
+      err);
   return cudaGetLastError();
 }
 
@@ -811,10 +956,21 @@ cudaError_t launch_compact(const int32_t* row_ok, int64_t N, int32_t* rows, Ctrl
 }
 
 cudaError_t launch_gather_rows(const void* h, size_t elem, int64_t d, const ChunkArgs& a,
-                               void* hc, cudaStream_t s) {
-  gather_rows_kernel<<<static_cast<unsigned>(round_up(a.chunk, 128)), 128, 0, s>>>(
+                               void* hc, const void* W, const int32_t* top1, float k2,
+                               cudaStream_t s) {
+  if (a.mref != nullptr && (elem != 2 || W == nullptr || top1 == nullptr))
+    return cudaErrorInvalidValue;
+  gather_rows_kernel<<<static_cast<unsigned>(round_up(a.chunk, 128)), kGatherThreads, 0, s>>>(
       static_cast<const uint8_t*>(h), d * static_cast<int64_t>(elem), a,
-      static_cast<uint8_t*>(hc));
+      static_cast<uint8_t*>(hc), static_cast<const uint8_t*>(W), top1, k2);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_grad_prepare(const ChunkArgs& a, uint16_t* u, uint16_t* hc, int64_t d,
+                                cudaStream_t s) {
+  if (a.alpha_row == nullptr || d % 8 != 0) return cudaErrorInvalidValue;
+  grad_prepare_kernel<<<static_cast<unsigned>(round_up(a.chunk, 64)), kPrepGradThreads, 0, s>>>(
+      a, u, hc, d);
   return cudaGetLastError();
 }
 

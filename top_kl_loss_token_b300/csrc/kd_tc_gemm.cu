@@ -123,6 +123,7 @@ struct KParams {
   uint32_t tx_bytes[2];  // bytes one pipeline stage receives in both CTAs together
   float* out[2];
   int64_t ldo[2];
+  const float* row_scale[2];  // optional per-output-row factor (row m of the problem)
   int vec_ok[2];
   const int32_t* row_map[2];
   int64_t row_map_off[2];
@@ -152,6 +153,8 @@ struct KParams {
   float* part_ps;
   uint16_t* u;
   int64_t ldg;
+  const float* mref;     // [cpad] row references (nullptr: each block its own maximum)
+  int32_t* row_flag;     // [cpad] set when a block of the row keeps its own maximum
   // top-K cache epilogues (rows are the chunk's positions, columns the vocabulary)
   uint64_t* bkey;        // [count][bkey_ld] largest rank key of each 128-column block
   int64_t bkey_ld;
@@ -534,6 +537,16 @@ __device__ void epilogue_store(const KParams& P, const Sizes& S, Ctl* ctl, uint3
     const int col0 = tl.n * S.bn[pi] + half * 128;
     const int ncols = min(S.bn[pi] - half * 128, S.N[pi] - col0);  // columns of this half
     if (i < S.M[pi] && ncols > 0) {
+      if (P.row_scale[pi] != nullptr) {
+        const float f = P.row_scale[pi][i];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          v0[j] *= f;
+          v1[j] *= f;
+          v2[j] *= f;
+          v3[j] *= f;
+        }
+      }
       const int64_t orow =
           P.row_map[pi] != nullptr ? P.row_map[pi][P.row_map_off[pi] + i] : static_cast<int64_t>(i);
       float* dst = P.out[pi] + orow * P.ldo[pi] + col0;
@@ -614,12 +627,14 @@ __device__ void epilogue_pass1(const KParams& P, const Sizes& S, Ctl* ctl, uint3
     int lo = 0, hi = 0;
     const int32_t* lidx = nullptr;
     const float* lp = nullptr;
+    float mr = 0.f;  // the row's reference (loaded before the accumulator wait)
     if (live) {
       lo = P.boff[static_cast<int64_t>(pb) * P.cpad + i];
       hi = P.boff[static_cast<int64_t>(pb + 1) * P.cpad + i];
       const int64_t r = P.rows[P.row0 + i];
       lidx = P.idx_sorted + r * P.K_top;
       lp = P.p_sorted + r * P.K_top;
+      if (P.mref != nullptr) mr = P.mref[i];
     }
 
     ok = mbar_wait(&ctl->tfull[b], tp, wc);
@@ -658,10 +673,18 @@ __device__ void epilogue_pass1(const KParams& P, const Sizes& S, Ctl* ctl, uint3
       const int64_t off = static_cast<int64_t>(i) * P.ldg + col0;
       float l = 0.f;
       float m2;
+      // The block's exponentials are taken relative to the row's reference
+      // when its maximum is at most kRefSlack above it (then every block of
+      // the row shares one reference and the gradient products can use the
+      // stored values directly), else relative to its own maximum.
       if (nv == 128) {
         const float mx = fmaxf(fmaxf(max32(v0, 32, false), max32(v1, 32, false)),
                                fmaxf(max32(v2, 32, false), max32(v3, 32, false)));
         m2 = mx * k2;
+        if (P.mref != nullptr) {
+          if (m2 - mr <= kRefSlack) m2 = mr;
+          else P.row_flag[i] = 1;
+        }
         lse_chunk32<false>(v0, 32, k2, m2, l, P.u, off);
         lse_chunk32<false>(v1, 32, k2, m2, l, P.u, off + 32);
         lse_chunk32<false>(v2, 32, k2, m2, l, P.u, off + 64);
@@ -670,6 +693,10 @@ __device__ void epilogue_pass1(const KParams& P, const Sizes& S, Ctl* ctl, uint3
         const float mx = fmaxf(fmaxf(max32(v0, nv, true), max32(v1, nv - 32, true)),
                                fmaxf(max32(v2, nv - 64, true), max32(v3, nv - 96, true)));
         m2 = mx * k2;
+        if (P.mref != nullptr) {
+          if (m2 - mr <= kRefSlack) m2 = mr;
+          else P.row_flag[i] = 1;
+        }
         lse_chunk32<true>(v0, nv, k2, m2, l, P.u, off);
         lse_chunk32<true>(v1, nv - 32, k2, m2, l, P.u, off + 32);
         lse_chunk32<true>(v2, nv - 64, k2, m2, l, P.u, off + 64);
@@ -1115,6 +1142,7 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& g, cudaStream_t s) {
     P.vec_ok[pi] = (q.ldo % 4 == 0) && (reinterpret_cast<uintptr_t>(q.out) % 16 == 0);
     P.row_map[pi] = q.row_map;
     P.row_map_off[pi] = q.row_map_off;
+    P.row_scale[pi] = q.row_scale;
     P.accumulate[pi] = q.accumulate;
     P.count_mode[pi] = q.count_mode;
   }
@@ -1167,6 +1195,11 @@ cudaError_t launch_tc_pass1(const Pass1Args& p, const ChunkArgs& a, cudaStream_t
   P.part_ps = a.part_ps;
   P.u = p.u;
   P.ldg = a.ldg;
+  if (p.row_ref) {
+    if (a.mref == nullptr || a.row_flag == nullptr || p.u == nullptr) return cudaErrorInvalidValue;
+    P.mref = a.mref;
+    P.row_flag = a.row_flag;
+  }
   cudaError_t e = cudaMemsetAsync(p.counter, 0, sizeof(uint32_t), s);
   if (e != cudaSuccess) return e;
   return launch_mode<kModePass1>(P, p.num_sms, s);
