@@ -99,7 +99,7 @@ def measured_traffic(kernel: str, workload: str, chunk: int):
     return int(b.group(1))
 
 
-def hbm_kernel_bytes(x, chunk: int, valid: int) -> dict:
+def hbm_kernel_bytes(x, chunk: int, valid: int, grads: bool = True) -> dict:
     """Algorithmic DRAM bytes per launch of the bandwidth-bound kernels (each
     input read once, each output written once)."""
     N, d, V, K = x.N, x.d, x.V, x.K
@@ -108,17 +108,23 @@ def hbm_kernel_bytes(x, chunk: int, valid: int) -> dict:
     c = min(chunk, valid) if valid else 0
     n_chunks = max(1, -(-valid // chunk)) if valid else 1
     c_avg = valid / n_chunks if valid else 0
+    elem = 2 if x.dtype == "bf16" else 4
     return {
         # topk_idx and topk_logit read, sorted (index, p) lists written
         "teacher_prep": 16.0 * N * K,
-        # u read and G written (bf16), per-(row, block) alpha and offsets, sorted lists
-        "grad_tile": c_avg * (4.0 * ldg + 6.0 * n_pb + 8.0 * K),
+        # fp32 path: u read and G written, per-(row, block) alpha and offsets, sorted lists
+        "grad_tile": c_avg * (2.0 * elem * ldg + 6.0 * n_pb + 8.0 * K),
+        # bf16 path: the chunk's h row read and written, the sorted lists read,
+        # one stored value read and written per teacher entry, three row factors
+        "grad_prepare": c_avg * (2.0 * elem * d + 8.0 * K + 4.0 * K + 12.0),
         # three per-(row, block) statistics read, alpha written
         "lse_combine": c_avg * 16.0 * n_pb,
         # sorted indices read, per-(row, block) offsets written
         "bucket_offsets": c_avg * (4.0 * K + 2.0 * (n_pb + 1)),
         # the chunk's h rows read and written contiguously
-        "gather_rows": c_avg * 4.0 * d,
+        # (bf16 with gradients: also the W row of the teacher's top entry, for
+        # the row's exponential reference)
+        "gather_rows": c_avg * (2.0 * elem * d + (elem * d if grads and elem == 2 else 0.0)),
     }
 
 
@@ -554,6 +560,25 @@ def _torch_kl_sum(h, W, idx, lg, T):
     return (logp.exp() * (logp - logq.gather(1, idx.long()))).sum()
 
 
+def torch_kl_arm(h, W, idx, lg, T, chunk=0):
+    """One of the pages' two plain-PyTorch baselines for the memory comparison:
+    the dense KL (chunk <= 0: the whole N x V logit grid built at once and kept
+    for autograd) or the forward-chunked KL (the grid built chunk by chunk in
+    the forward, every chunk's grid still kept for the one backward).  Returns
+    (loss = mean over the rows, grad_h, grad_W) from autograd."""
+    h = h.detach().requires_grad_(True)
+    W = W.detach().requires_grad_(True)
+    N = h.shape[0]
+    if chunk <= 0:
+        tot = _torch_kl_sum(h, W, idx, lg, T)
+    else:
+        tot = sum(_torch_kl_sum(h[r:r + chunk], W, idx[r:r + chunk], lg[r:r + chunk], T)
+                  for r in range(0, N, chunk))
+    loss = tot / N
+    loss.backward()
+    return loss.detach(), h.grad, W.grad
+
+
 def run_dense_context(args):
     """Context for the pages' peak-memory comparison (dense KL, forward-chunked
     KL, fused chunked KL): peak device memory and time of one fwd+bwd of the
@@ -611,22 +636,12 @@ def run_dense_context(args):
                                    grad_W=gW, workspace=ws)
                     rec["grad_dtype"] = "fp32"
                 else:
-                    h = h0.detach().requires_grad_(True)
-                    W = W0.detach().requires_grad_(True)
                     out = {}
 
                     def fn():
-                        h.grad = None
-                        W.grad = None
-                        if arm == "dense":
-                            tot = _torch_kl_sum(h, W, idx, lg, T)
-                        else:
-                            tot = sum(_torch_kl_sum(h[r:r + chunk], W, idx[r:r + chunk],
-                                                    lg[r:r + chunk], T)
-                                      for r in range(0, N, chunk))
-                        loss_t = tot / N
-                        loss_t.backward()
-                        out["loss"] = loss_t.detach()
+                        out.clear()
+                        out["loss"], out["gh"], out["gW"] = torch_kl_arm(
+                            h0, W0, idx, lg, T, 0 if arm == "dense" else chunk)
                     rec["grad_dtype"] = "bf16"
                 rec["ms"] = timed(fn)
                 torch.cuda.synchronize(dev)
@@ -637,7 +652,7 @@ def run_dense_context(args):
                 rec["outcome"] = "out of device memory"
             rec["inputs_gib"] = base / 2 ** 30
             rows.append(rec)
-            loss = gh = gW = ws = h = W = out = fn = None  # release this arm's buffers
+            loss = gh = gW = ws = out = fn = None  # release this arm's buffers
             torch.cuda.synchronize(dev)
             torch.cuda.empty_cache()
         del h0, idx, lg
@@ -858,7 +873,7 @@ def main():
                 "avg_launch_ms": tot_ms / launches}
     launches_total = sum(v[0] for v in kernels.values())
     hbm = {}
-    for name, nbytes in hbm_kernel_bytes(x, chunk, valid_tokens).items():
+    for name, nbytes in hbm_kernel_bytes(x, chunk, valid_tokens, grads=not args.fwd).items():
         if name not in kernels:
             continue
         launches, tot_ms = kernels[name]
