@@ -864,7 +864,8 @@ def main():
         achieved = flops_per_launch / (tot_ms / launches / 1000.0) / 1e12
         peak = peaks["bf16_tflops_sustained"]
         traffic = None
-        if not args.tokens and args.config == 3:
+        if not args.tokens and args.config == 3 and not args.fwd:
+            # the capture is of the fwd+bwd launches (pass 1 storing its exponentials)
             traffic = measured_traffic(dom, x.name, chunk)
         roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
