@@ -231,6 +231,13 @@ cudaError_t launch_simt_gemm(const SimtGemm& g, cudaStream_t s);
 bool encode_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                       uint64_t ld_elems, uint32_t box_inner, uint32_t box_outer);
 
+// Tensor map of an output written by TMA stores from the 128-byte swizzle
+// layout: fp32 (f32) or bf16 elements, [outer][inner] row-major with leading
+// dimension ld_elems, one box = box_inner x box_outer (box_inner * element
+// size = 128 bytes).
+bool encode_tmap_store(CUtensorMap* m, const void* base, bool f32, uint64_t inner, uint64_t outer,
+                       uint64_t ld_elems, uint32_t box_inner, uint32_t box_outer);
+
 // An MN-major bf16 operand stored [outer = K][inner = MN] (MN contiguous,
 // inner a multiple of 64), viewed as [inner / 64][outer][64] so that one box
 // of `atoms` x box_k x 64 brings `atoms` consecutive 64-element atoms in the

@@ -47,7 +47,11 @@
 //               per CTA); in the first CTA one lane issues the pair MMAs
 //               (256 x N x 16, bf16 in, fp32 out);
 //   warps 2-9   epilogue: each warp reads 32 TMEM lanes (rows) x 128 columns
-//               of its own CTA's accumulator.
+//               of its own CTA's accumulator.  Large contiguous outputs (pass
+//               1's stored exponentials, plain GEMM results) go out through a
+//               4 KiB staging buffer per warp and TMA stores (adds when
+//               accumulating), 32 rows x 128 bytes per store; those modes keep
+//               6 ring stages instead of 7 to make room.
 // Operands are staged in the 128-byte swizzle layout; a K-major operand tile
 // is one TMA box of 64 x rows, an MN-major tile is made of 64 x 64 atoms,
 // brought by one 3-D box when the tile starts on an atom boundary.
@@ -67,7 +71,7 @@ constexpr int kEpiWarps = 8;
 constexpr int kBProducerWarp = 2 + kEpiWarps;    // warp 10
 constexpr int kThreads = (3 + kEpiWarps) * 32;
 constexpr int kSched = 4;
-constexpr int kStages = 7;
+constexpr int kMaxStages = 7;
 constexpr int kPairM = 2 * kBM;                 // rows of a pair's output tile
 constexpr uint32_t kTmemCols = 2 * kBN;
 constexpr int kABytes = kBM * kBK * 2;          // this CTA's 128 rows of A
@@ -78,8 +82,8 @@ constexpr int kAtomBytes = 64 * kBK * 2;  // one 64 (MN) x 64 (K) box of an MN-m
 // Barriers and the tile ring.  In the pair's second CTA, full[], tempty[] and
 // sempty[] are unused: those waits happen in the first CTA.
 struct Ctl {
-  uint64_t full[kStages];   // first CTA: both CTAs' operands of a stage landed
-  uint64_t empty[kStages];  // each CTA: the pair MMAs reading a stage are done
+  uint64_t full[kMaxStages];   // first CTA: both CTAs' operands of a stage landed
+  uint64_t empty[kMaxStages];  // each CTA: the pair MMAs reading a stage are done
   uint64_t tfull[2];        // each CTA: accumulator b is complete
   uint64_t tempty[2];       // first CTA: both CTAs' epilogues have read accumulator b
   uint64_t sfull[kSched];   // each CTA: a tile number is in sched_tile[slot]
@@ -90,8 +94,33 @@ struct Ctl {
   int abort;
 };
 
-constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStages) * kStageBytes + sizeof(Ctl);
-static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+enum : int {
+  kModePass1 = 0,     // student logits + top-K statistics (the loss against the cache)
+  kModeStore = 1,     // plain GEMMs, fp32 results stored or accumulated
+  kModeTopkMax = 2,   // teacher top-K cache, pass 1
+  kModeTopkCand = 3,  // teacher top-K cache, pass 2
+  kModeDual = 4       // full-vocabulary loss: teacher then student logits of one tile
+};
+
+// Output staging: an epilogue warp writes its results 32 rows x 128 bytes at
+// a time into its own shared-memory buffer (128-byte swizzle layout) and a
+// TMA store (or reduce-add) moves the buffer to global memory, so the
+// results leave the SM as whole lines instead of one 16-byte piece per row
+// and thread.  The modes that write large outputs this way (pass 1: the
+// stored exponentials; plain GEMMs: contiguous fp32 results) give one ring
+// stage to the staging buffers.
+constexpr int kStageWarpBytes = 32 * 128;
+constexpr int kStagingBytes = kEpiWarps * kStageWarpBytes;
+
+template <int MODE>
+struct ModeCfg {
+  static constexpr bool kStaged = MODE == kModePass1 || MODE == kModeStore;
+  static constexpr int kStages = kStaged ? kMaxStages - 1 : kMaxStages;
+  static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * kStageBytes +
+                                  (kStaged ? kStagingBytes : 0) + sizeof(Ctl);
+};
+static_assert(ModeCfg<kModeStore>::kSmem <= 232448, "shared memory per CTA");
+static_assert(ModeCfg<kModeDual>::kSmem <= 232448, "shared memory per CTA");
 
 // Arrivals that complete one phase of the first CTA's barriers.
 constexpr uint32_t kTemptyCount = 2 * kEpiWarps;          // epilogue warps of both CTAs
@@ -105,17 +134,14 @@ enum : int {
   kLoadMN3d = 2   // MN-major, atom-aligned: one 3-D box covering every atom
 };
 
-enum : int {
-  kModePass1 = 0,     // student logits + top-K statistics (the loss against the cache)
-  kModeStore = 1,     // plain GEMMs, fp32 results stored or accumulated
-  kModeTopkMax = 2,   // teacher top-K cache, pass 1
-  kModeTopkCand = 3,  // teacher top-K cache, pass 2
-  kModeDual = 4       // full-vocabulary loss: teacher then student logits of one tile
-};
-
 struct KParams {
   CUtensorMap tmA[2];
   CUtensorMap tmB[2];
+  // staged outputs: kModeStore problem pi's result [M, N] fp32 (out_tma[pi] = 1:
+  // stored, 2: added), kModePass1's stored exponentials [cpad, ldg] bf16 in
+  // tmOut[0] (out_tma[0] = 1); 0: no staged output
+  CUtensorMap tmOut[2];
+  int out_tma[2];
   int a_mn[2], b_mn[2];
   int a_load[2], b_load[2];  // kLoadK / kLoadMN2d / kLoadMN3d
   int M[2], N[2], K[2];
@@ -174,10 +200,12 @@ struct Sizes {
   int M[2], N[2], nkb[2], mt[2], nt[2], tiles[2], bn[2], b3d[2];
   int total;
   int count;
+  int group_m;  // plain GEMMs: tile rows per raster group (0: row order)
 };
 
 __device__ __forceinline__ Sizes get_sizes(const KParams& P) {
   Sizes s;
+  s.group_m = P.nprob == 1 ? 8 : 0;
   int count = P.chunk;
   if (P.n_valid != nullptr) {
     const long long c = static_cast<long long>(*P.n_valid) - P.row0;
@@ -219,7 +247,11 @@ struct Tile {
 
 // Pass 1 walks the vocabulary slowly (m fastest) so that the CTAs running at
 // the same time share one W tile; the backward walks the output columns
-// fastest so that the CTAs running together share one A (G) slab.
+// fastest so that the CTAs running together share one A (G) slab.  A plain
+// GEMM (one problem) goes through its output in groups of 8 tile rows, m
+// fastest within a group, so that the tiles running together share both
+// operands' tiles in L2 (measured at 8192^3: 1543-1555 against 1473-1479
+// TFLOP/s with plain row order).
 template <int MODE>
 __device__ __forceinline__ Tile decode_tile(const Sizes& S, int t) {
   Tile tl;
@@ -232,6 +264,13 @@ __device__ __forceinline__ Tile decode_tile(const Sizes& S, int t) {
   if (MODE == kModePass1 || MODE == kModeTopkMax || MODE == kModeTopkCand || MODE == kModeDual) {
     tl.m = t % S.mt[pi];
     tl.n = t / S.mt[pi];
+  } else if (S.group_m > 0 && S.mt[pi] > S.group_m) {
+    const int per = S.group_m * S.nt[pi];
+    const int m0 = (t / per) * S.group_m;
+    const int r = t % per;
+    const int gsz = min(S.group_m, S.mt[pi] - m0);
+    tl.m = m0 + r % gsz;
+    tl.n = r / gsz;
   } else {
     tl.n = t % S.nt[pi];
     tl.m = t / S.nt[pi];
@@ -354,7 +393,7 @@ __device__ void producer_loop(const KParams& P, const Sizes& S, uint8_t* smem, C
       const CUtensorMap* m = OPERAND == 0 ? &P.tmA[pk] : &P.tmB[pk];
       const int mode = OPERAND == 0 ? P.a_load[pk] : P.b_load[pk];
       load_operand(dst, m, mode, fb, mn0, mn_count, (kb < nkb0 ? kb : kb - nkb0) * kBK);
-      if (++stage == kStages) {
+      if (++stage == ModeCfg<MODE>::kStages) {
         stage = 0;
         phase ^= 1u;
       }
@@ -440,7 +479,7 @@ __device__ void mma_loop(const KParams& P, const Sizes& S, uint8_t* smem, Ctl* c
         umma_bf16_pair(d_tmem, ad, bd, idesc, (kb_in > 0 || kk > 0) ? 1u : 0u);
       }
       umma_commit_pair_both(&ctl->empty[stage]);
-      if (++stage == kStages) {
+      if (++stage == ModeCfg<MODE>::kStages) {
         stage = 0;
         phase ^= 1u;
       }
@@ -492,8 +531,39 @@ __device__ __forceinline__ void store_chunk32(float* dst, const float (&v)[32], 
   }
 }
 
+// Writes one piece of 32 rows x 128 bytes, held one row per lane as 32 words,
+// into the warp's staging buffer in the 128-byte swizzle layout of the
+// output's tensor map, then lane 0 stores it (or adds it) at (x, y) with TMA
+// and waits until the buffer has been read, so the next piece may reuse it.
+// The rows and columns of the box that fall outside the tensor are dropped
+// by the TMA unit.
+__device__ __forceinline__ void stage_piece(const CUtensorMap* m, uint8_t* buf,
+                                            const uint32_t (&w)[32], int lane, int x, int y,
+                                            bool add) {
+  const uint32_t row = smem_u32(buf) + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    st_shared_v4(row + ((static_cast<uint32_t>(c) ^ (static_cast<uint32_t>(lane) & 7u)) << 4),
+                 w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    if (add) tma_reduce_add_2d(m, buf, x, y);
+    else tma_store_2d(m, buf, x, y);
+    bulk_commit_group();
+    bulk_wait_group_read0();
+  }
+  __syncwarp();
+}
+
+__device__ __forceinline__ void stage_f32(const CUtensorMap* m, uint8_t* buf, const float (&v)[32],
+                                          int lane, int x, int y, bool add) {
+  const uint32_t (&w)[32] = *reinterpret_cast<const uint32_t(*)[32]>(v);
+  stage_piece(m, buf, w, lane, x, y, add);
+}
+
 __device__ void epilogue_store(const KParams& P, const Sizes& S, Ctl* ctl, uint32_t tmem,
-                               const WaitCtx& wc, int warp, int lane, int rank) {
+                               const WaitCtx& wc, int warp, int lane, int rank, uint8_t* wbuf) {
   const int q = warp & 3;           // TMEM lane quarter this warp may read
   const int half = (warp - 2) >> 2; // which 128 columns of the 256
   int slot = 0;
@@ -533,10 +603,20 @@ __device__ void epilogue_store(const KParams& P, const Sizes& S, Ctl* ctl, uint3
     __syncwarp();
     if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->tempty[b]), 0));
 
-    const int i = tl.m * kPairM + rank * kBM + q * 32 + lane;
+    const int i0 = tl.m * kPairM + rank * kBM + q * 32;  // the warp's first row
+    const int i = i0 + lane;
     const int col0 = tl.n * S.bn[pi] + half * 128;
     const int ncols = min(S.bn[pi] - half * 128, S.N[pi] - col0);  // columns of this half
-    if (i < S.M[pi] && ncols > 0) {
+    if (P.out_tma[pi] != 0) {
+      // contiguous fp32 result: staged, whole-line TMA stores (or adds)
+      if (i0 < S.M[pi] && ncols > 0) {
+        const bool add = P.out_tma[pi] == 2;
+        stage_f32(&P.tmOut[pi], wbuf, v0, lane, col0, i0, add);
+        if (ncols > 32) stage_f32(&P.tmOut[pi], wbuf, v1, lane, col0 + 32, i0, add);
+        if (ncols > 64) stage_f32(&P.tmOut[pi], wbuf, v2, lane, col0 + 64, i0, add);
+        if (ncols > 96) stage_f32(&P.tmOut[pi], wbuf, v3, lane, col0 + 96, i0, add);
+      }
+    } else if (i < S.M[pi] && ncols > 0) {
       if (P.row_scale[pi] != nullptr) {
         const float f = P.row_scale[pi][i];
 #pragma unroll
@@ -559,15 +639,18 @@ __device__ void epilogue_store(const KParams& P, const Sizes& S, Ctl* ctl, uint3
       if (nc > 96) store_chunk32(dst + 96, v3, nc - 96, vec, acc);
     }
   }
+  // every staged store complete before the kernel ends
+  if (lane == 0) bulk_wait_group0();
+  __syncwarp();
 }
 
 // Logsumexp statistics of 32 consecutive logits of one row, in base-2 units
-// s2 = z * k2 relative to the block max m2; exponentials stored as bf16.
-// (u == nullptr: the loss alone, nothing is stored)
+// s2 = z * k2 relative to the block's reference m2: the sum of the
+// exponentials into l, and the exponentials themselves as 16 words of two
+// bf16 (lower column in the low half) into w, for the staged store.
 template <bool kMasked>
 __device__ __forceinline__ void lse_chunk32(const float (&v)[32], int nvalid, float k2, float m2,
-                                            float& l, uint16_t* u, int64_t off) {
-  uint32_t w[16];
+                                            float& l, uint32_t* w) {
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     float e0 = ex2_approx(fmaf(v[2 * j], k2, -m2));
@@ -579,10 +662,6 @@ __device__ __forceinline__ void lse_chunk32(const float (&v)[32], int nvalid, fl
     l += e0 + e1;
     w[j] = pack_bf16x2(e0, e1);
   }
-  if (u == nullptr) return;
-  uint4* d4 = reinterpret_cast<uint4*>(u + off);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) d4[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
 }
 
 __device__ __forceinline__ float max32(const float (&v)[32], int nvalid, bool masked) {
@@ -595,7 +674,7 @@ __device__ __forceinline__ float max32(const float (&v)[32], int nvalid, bool ma
 }
 
 __device__ void epilogue_pass1(const KParams& P, const Sizes& S, Ctl* ctl, uint32_t tmem,
-                               const WaitCtx& wc, int warp, int lane, int rank) {
+                               const WaitCtx& wc, int warp, int lane, int rank, uint8_t* wbuf) {
   const int q = warp & 3;
   const int half = (warp - 2) >> 2;
   int slot = 0;
@@ -619,10 +698,12 @@ __device__ void epilogue_pass1(const KParams& P, const Sizes& S, Ctl* ctl, uint3
     const uint32_t tp = (static_cast<uint32_t>(it) >> 1) & 1u;
     ++it;
 
-    const int i = tl.m * kPairM + rank * kBM + q * 32 + lane;  // row within the chunk
+    const int i0 = tl.m * kPairM + rank * kBM + q * 32;      // the warp's first row
+    const int i = i0 + lane;                                   // row within the chunk
     const int col0 = tl.n * kBN + half * 128;  // first vocabulary column of this block
     const int pb = tl.n * 2 + half;            // 128-column block index
-    const bool live = (i < S.count) && (pb < P.n_pb);
+    const bool block_live = pb < P.n_pb;       // the same for the whole warp
+    const bool live = (i < S.count) && block_live;
     // Teacher entries of this row that fall in this column block.
     int lo = 0, hi = 0;
     const int32_t* lidx = nullptr;
@@ -668,46 +749,58 @@ __device__ void epilogue_pass1(const KParams& P, const Sizes& S, Ctl* ctl, uint3
     __syncwarp();
     if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->tempty[b]), 0));
 
-    if (live) {
+    // Every lane of a live block computes its row's exponentials (rows past
+    // the chunk's count hold values nobody reads: they are stored with the
+    // rest of the box, and cleared or ignored later); the statistics and the
+    // row flag are written for the chunk's rows only.
+    if (block_live && i0 < S.count) {
       const int nv = min(128, P.V - col0);
-      const int64_t off = static_cast<int64_t>(i) * P.ldg + col0;
       float l = 0.f;
       float m2;
       // The block's exponentials are taken relative to the row's reference
       // when its maximum is at most kRefSlack above it (then every block of
       // the row shares one reference and the gradient products can use the
       // stored values directly), else relative to its own maximum.
+      uint32_t wa[32], wb[32];  // columns 0-63 and 64-127, two bf16 per word
       if (nv == 128) {
         const float mx = fmaxf(fmaxf(max32(v0, 32, false), max32(v1, 32, false)),
                                fmaxf(max32(v2, 32, false), max32(v3, 32, false)));
         m2 = mx * k2;
-        if (P.mref != nullptr) {
+        if (live && P.mref != nullptr) {
           if (m2 - mr <= kRefSlack) m2 = mr;
           else P.row_flag[i] = 1;
         }
-        lse_chunk32<false>(v0, 32, k2, m2, l, P.u, off);
-        lse_chunk32<false>(v1, 32, k2, m2, l, P.u, off + 32);
-        lse_chunk32<false>(v2, 32, k2, m2, l, P.u, off + 64);
-        lse_chunk32<false>(v3, 32, k2, m2, l, P.u, off + 96);
+        lse_chunk32<false>(v0, 32, k2, m2, l, wa);
+        lse_chunk32<false>(v1, 32, k2, m2, l, wa + 16);
+        lse_chunk32<false>(v2, 32, k2, m2, l, wb);
+        lse_chunk32<false>(v3, 32, k2, m2, l, wb + 16);
       } else {
         const float mx = fmaxf(fmaxf(max32(v0, nv, true), max32(v1, nv - 32, true)),
                                fmaxf(max32(v2, nv - 64, true), max32(v3, nv - 96, true)));
         m2 = mx * k2;
-        if (P.mref != nullptr) {
+        if (live && P.mref != nullptr) {
           if (m2 - mr <= kRefSlack) m2 = mr;
           else P.row_flag[i] = 1;
         }
-        lse_chunk32<true>(v0, nv, k2, m2, l, P.u, off);
-        lse_chunk32<true>(v1, nv - 32, k2, m2, l, P.u, off + 32);
-        lse_chunk32<true>(v2, nv - 64, k2, m2, l, P.u, off + 64);
-        lse_chunk32<true>(v3, nv - 96, k2, m2, l, P.u, off + 96);
+        lse_chunk32<true>(v0, nv, k2, m2, l, wa);
+        lse_chunk32<true>(v1, nv - 32, k2, m2, l, wa + 16);
+        lse_chunk32<true>(v2, nv - 64, k2, m2, l, wb);
+        lse_chunk32<true>(v3, nv - 96, k2, m2, l, wb + 16);
       }
-      const int64_t o = static_cast<int64_t>(pb) * P.cpad + i;
-      P.part_m[o] = m2;
-      P.part_l[o] = l;
-      P.part_ps[o] = ps * k2;
+      if (P.out_tma[0] != 0) {  // the stored exponentials, through the staging buffer
+        stage_piece(&P.tmOut[0], wbuf, wa, lane, col0, i0, false);
+        stage_piece(&P.tmOut[0], wbuf, wb, lane, col0 + 64, i0, false);
+      }
+      if (live) {
+        const int64_t o = static_cast<int64_t>(pb) * P.cpad + i;
+        P.part_m[o] = m2;
+        P.part_l[o] = l;
+        P.part_ps[o] = ps * k2;
+      }
     }
   }
+  if (lane == 0) bulk_wait_group0();
+  __syncwarp();
 }
 
 // Rank key of logit z at vocabulary index v: a larger key ranks first.  The
@@ -972,7 +1065,8 @@ template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ KParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_smem(smem_raw);
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + kStages * kStageBytes);
+  uint8_t* staging = smem + ModeCfg<MODE>::kStages * kStageBytes;
+  Ctl* ctl = reinterpret_cast<Ctl*>(staging + (ModeCfg<MODE>::kStaged ? kStagingBytes : 0));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -982,7 +1076,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
 
   if (threadIdx.x == 0) {
 #pragma unroll
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < ModeCfg<MODE>::kStages; ++s) {
       mbar_init(&ctl->full[s], 1);
       mbar_init(&ctl->empty[s], 1);
     }
@@ -1026,10 +1120,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   } else if (warp == kBProducerWarp) {
     if (lane == 0) producer_loop<MODE, 1>(P, S, smem, ctl, wc, rank);
   } else {
+    uint8_t* wbuf = staging + (warp - 2) * kStageWarpBytes;  // this warp's staging buffer
     if (MODE == kModePass1)
-      epilogue_pass1(P, S, ctl, tmem, wc, warp, lane, static_cast<int>(rank));
+      epilogue_pass1(P, S, ctl, tmem, wc, warp, lane, static_cast<int>(rank), wbuf);
     else if (MODE == kModeStore)
-      epilogue_store(P, S, ctl, tmem, wc, warp, lane, static_cast<int>(rank));
+      epilogue_store(P, S, ctl, tmem, wc, warp, lane, static_cast<int>(rank), wbuf);
     else if (MODE == kModeDual)
       epilogue_dual(P, S, ctl, tmem, wc, warp, lane, static_cast<int>(rank));
     else
@@ -1051,7 +1146,7 @@ template <int MODE>
 cudaError_t launch_mode(const KParams& P, int num_sms, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<MODE>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kSmemBytes));
+                                       static_cast<int>(ModeCfg<MODE>::kSmem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));
@@ -1061,7 +1156,7 @@ cudaError_t launch_mode(const KParams& P, int num_sms, cudaStream_t s) {
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = ModeCfg<MODE>::kSmem;
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
@@ -1143,6 +1238,14 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& g, cudaStream_t s) {
     P.row_map[pi] = q.row_map;
     P.row_map_off[pi] = q.row_map_off;
     P.row_scale[pi] = q.row_scale;
+    // a contiguous result (no row map, no row factor) leaves through the
+    // staging buffers as whole-line TMA stores, or adds when accumulating
+    if (q.row_map == nullptr && q.row_scale == nullptr && (q.ldo * 4) % 16 == 0 &&
+        (reinterpret_cast<uintptr_t>(q.out) & 15u) == 0) {
+      if (!encode_tmap_store(&P.tmOut[pi], q.out, true, q.N, q.M, q.ldo, 32, 32))
+        return cudaErrorInvalidValue;
+      P.out_tma[pi] = q.accumulate ? 2 : 1;
+    }
     P.accumulate[pi] = q.accumulate;
     P.count_mode[pi] = q.count_mode;
   }
@@ -1195,6 +1298,11 @@ cudaError_t launch_tc_pass1(const Pass1Args& p, const ChunkArgs& a, cudaStream_t
   P.part_ps = a.part_ps;
   P.u = p.u;
   P.ldg = a.ldg;
+  if (p.u != nullptr) {  // the stored exponentials leave through the staging buffers
+    if (!encode_tmap_store(&P.tmOut[0], p.u, false, a.ldg, a.cpad, a.ldg, 64, 32))
+      return cudaErrorInvalidValue;
+    P.out_tma[0] = 1;
+  }
   if (p.row_ref) {
     if (a.mref == nullptr || a.row_flag == nullptr || p.u == nullptr) return cudaErrorInvalidValue;
     P.mref = a.mref;
