@@ -58,11 +58,12 @@ extern "C" {
  *                          relative to one reference, minus the teacher's
  *                          probabilities scaled to match
  *   rowstat:    fp32 [4, N] (KD_BF16 with gradients), for the i-th valid row
- *               of the call (every chunk, compacted order): [0] its reference
- *               m_i (log2 units), [1] (int32) 1 if some vocabulary block kept
- *               its own maximum as reference, [2] alpha_i, [3] 1 / (alpha_i T
+ *               of the call (every chunk, compacted order): [0] the common
+ *               reference M_i (log2 units) of its stored values, [1] (int32) 1
+ *               if some vocabulary block kept its own maximum as reference (the
+ *               row was then rescaled to M_i), [2] alpha_i, [3] 1 / (alpha_i T
  *               N_valid); alpha_i of the last chunk's row i is at
- *               [2, j * chunk + i]
+ *               [2, j * chunk + i]; part_m holds each block's reference
  *   hc:         [chunk_pad, d] the chunk's rows of h (KD_BF16 with gradients:
  *               multiplied by alpha_i and rounded to bf16, so that grad_W
  *               receives g'^T hc)

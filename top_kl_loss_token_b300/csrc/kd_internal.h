@@ -147,7 +147,8 @@ struct ChunkArgs {
   // One reference per row (bf16 path with gradients; nullptr otherwise),
   // indexed by the chunk's row i (the arrays start at the chunk's first row):
   float* mref;           // row i's reference m_i (log2 units): the student's
-                         // logit at the teacher's most probable entry
+                         // logit at the teacher's most probable entry; after
+                         // the logsumexp combine, the row's common reference M_i
   int32_t* row_flag;     // 1: some block of row i kept its own maximum
   float* alpha_row;      // 2^(M_i - lse2_i) / (T n): dL/dz = alpha_row * stored tile
   float* beta_row;       // 2^(lse2_i - M_i)

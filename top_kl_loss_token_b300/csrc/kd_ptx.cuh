@@ -184,25 +184,36 @@ __device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* m
       : "memory");
 }
 
+// An L2 cache policy that evicts the lines it tags first: for streamed
+// outputs, which no kernel of the same launch reads again, so that they do
+// not push the operands out of L2.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 // Tiled store of one box from this CTA's shared memory (128-byte swizzle
 // layout of the tensor map) to global memory, tracked by the issuing thread's
-// bulk-async group.  x is the innermost coordinate; never negative here.
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, const void* src, int x, int y) {
+// bulk-async group, with the L2 cache policy `pol`.  x is the innermost
+// coordinate; never negative here.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, const void* src, int x, int y,
+                                             uint64_t pol) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;" ::"l"(
           reinterpret_cast<uint64_t>(m)),
-      "r"(smem_u32(src)), "r"(x), "r"(y)
+      "r"(smem_u32(src)), "r"(x), "r"(y), "l"(pol)
       : "memory");
 }
 
 // Same, adding the box element-wise into global memory (fp32 add, done by the
 // memory system) instead of overwriting it.
 __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* m, const void* src, int x,
-                                                  int y) {
+                                                  int y, uint64_t pol) {
   asm volatile(
-      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;" ::"l"(
           reinterpret_cast<uint64_t>(m)),
-      "r"(smem_u32(src)), "r"(x), "r"(y)
+      "r"(smem_u32(src)), "r"(x), "r"(y), "l"(pol)
       : "memory");
 }
 

@@ -416,11 +416,16 @@ __global__ void __launch_bounds__(kLseRows * kLseGroups) lse_kernel(
     if (a.alpha_row != nullptr) {
       // MM is the row's common reference: its own m_i, or, when some block
       // kept its own maximum, the largest block reference (the row is then
-      // rescaled to it before the gradient products)
+      // rescaled to it before the gradient products); it replaces m_i
       a.alpha_row[i] = ex2_approx(MM - lse2) * grad_scale(a.n_norm, T);
       a.beta_row[i] = ex2_approx(lse2 - MM);
+      a.mref[i] = MM;
     }
   }
+  // One reference per row: the gradient products need no per-block factor
+  // (grad_prepare rescales the rare rows with several references from the
+  // block references themselves).
+  if (a.alpha_row != nullptr) return;
   __syncthreads();
   if (!live) return;
   const float lse2 = sLse[x];
@@ -550,13 +555,14 @@ __global__ void __launch_bounds__(kPrepGradThreads) grad_prepare_kernel(
        v0 += kPrepGradThreads * 8)
     *reinterpret_cast<uint4*>(row + v0) = make_uint4(0u, 0u, 0u, 0u);
   const float ar = a.alpha_row[i];
-  if (a.row_flag[i] != 0 && ar > 0.f) {
+  if (a.row_flag[i] != 0) {
     // Some blocks of this row kept their own maximum as reference: bring every
-    // block to the row's common reference M (alpha_b / alpha_row =
-    // 2^(ref_b - M), at most 1).
+    // block to the row's common reference M (a factor 2^(ref_b - M), at most 1).
+    const float M = a.mref[i];
     for (int pb = tid; pb < a.n_pb; pb += kPrepGradThreads) {
-      const float f = a.part_m[static_cast<int64_t>(pb) * a.cpad + i] / ar;
-      if (f == 1.0f) continue;
+      const float rb = a.part_m[static_cast<int64_t>(pb) * a.cpad + i];
+      if (rb == M) continue;
+      const float f = ex2_approx(rb - M);
       uint4* p4 = reinterpret_cast<uint4*>(row + static_cast<int64_t>(pb) * kPB);
 #pragma unroll 4
       for (int q = 0; q < kPB / 8; ++q) {

@@ -548,8 +548,12 @@ __device__ __forceinline__ void stage_piece(const CUtensorMap* m, uint8_t* buf,
   fence_proxy_async_smem();
   __syncwarp();
   if (lane == 0) {
-    if (add) tma_reduce_add_2d(m, buf, x, y);
-    else tma_store_2d(m, buf, x, y);
+    // streamed outputs: evict-first in L2, so that they leave room for the
+    // operands (measured: pass 1 reads 2.95 instead of 3.44 GB of W per
+    // 8192-token chunk)
+    const uint64_t pol = l2_evict_first_policy();
+    if (add) tma_reduce_add_2d(m, buf, x, y, pol);
+    else tma_store_2d(m, buf, x, y, pol);
     bulk_commit_group();
     bulk_wait_group_read0();
   }
