@@ -55,9 +55,9 @@ def stored_tile(kd, got, dtype, N, row0, count, cpad, ldg):
     return g[:count]
 
 
-def teacher_case():
+def teacher_case(K=16):
     # duplicates, out-of-range indices and -inf logits in valid rows, plus masked rows
-    x = synth.make_inputs(300, 64, 1100, 16, T=1.5, dtype="bf16", seed=201, mask="random0.2")
+    x = synth.make_inputs(300, 64, 1100, K, T=1.5, dtype="bf16", seed=201, mask="random0.2")
     rng = np.random.default_rng(7)
     x.mask[:12] = 1
     x.idx[0, 3] = x.idx[0, 5]
@@ -65,13 +65,16 @@ def teacher_case():
     x.idx[2, 7] = 1100
     x.idx[3, 0] = -1
     x.logit[4, 2] = -np.inf
-    x.idx[5] = rng.integers(0, 20, size=16)
+    x.idx[5] = rng.integers(0, 20, size=K)
     return x
 
 
-def test_teacher_preparation(kd):
+# K <= 128 runs one warp per row (entries in registers, 1, 2 or 4 per lane);
+# larger K one block per row with the entries in shared memory
+@pytest.mark.parametrize("K", [16, 9, 33, 100, 128, 200])
+def test_teacher_preparation(kd, K):
     import torch
-    x = teacher_case()
+    x = teacher_case(K)
     got = run_gpu(kd, x, want_grads=False)
     assert got["err"] == oracle.FLAG_INDEX_RANGE
     N, K, V = x.N, x.K, x.V

@@ -232,6 +232,147 @@ __global__ void __launch_bounds__(kPrepThreads) teacher_prep_kernel(
   }
 }
 
+// The same teacher preparation with one warp per row, for K <= 128: each lane
+// keeps E = P2 / 32 entries in registers (entry g = lane + 32 e), the
+// reductions are warp shuffles and the sort is a bitonic network across lanes
+// (shuffles) and registers (swaps), so no block-wide barrier is needed.  Four
+// rows per block.
+constexpr int kPrepWarpRows = 4;
+
+template <int E>
+__global__ void __launch_bounds__(32 * kPrepWarpRows) teacher_prep_warp_kernel(
+    const int32_t* __restrict__ idx, const float* __restrict__ logit,
+    const uint8_t* __restrict__ mask, int64_t N, int K, int64_t V, float k2,
+    int32_t* __restrict__ row_ok, int32_t* __restrict__ idx_sorted,
+    float* __restrict__ p_sorted, float* __restrict__ plogp, float* __restrict__ psum,
+    int32_t* __restrict__ top1, uint32_t* __restrict__ err) {
+  const int lane = threadIdx.x & 31;
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * kPrepWarpRows + (threadIdx.x >> 5);
+  if (r >= N) return;
+  if (mask != nullptr && mask[r] == 0) {
+    if (lane == 0) row_ok[r] = 0;
+    return;
+  }
+  const int32_t* ri = idx + r * K;
+  const float* rl = logit + r * K;
+  int key[E];
+  float val[E];
+  int bits = 0;  // 1: out of range seen, 2: NaN / +inf seen, 4: finite seen
+  float mx = -INFINITY;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int k = lane + 32 * e;
+    key[e] = kNoIndex;
+    val[e] = -INFINITY;
+    if (k < K) {
+      const int32_t v = ri[k];
+      const float l = rl[k];
+      if (v < 0 || static_cast<int64_t>(v) >= V) {
+        bits |= 1;
+      } else {
+        key[e] = v;
+        if (isnan(l) || l == INFINITY) bits |= 2;
+        if (isfinite(l)) bits |= 4;
+        val[e] = l * k2;
+        mx = fmaxf(mx, val[e]);
+      }
+    }
+  }
+  bits = warp_or(bits);
+  mx = warp_max(mx);
+  const bool bad = (bits & 2) || !(bits & 4);
+  if (lane == 0) {
+    uint32_t f = 0;
+    if (bits & 1) f |= KD_FLAG_INDEX_RANGE;
+    if (bad) f |= KD_FLAG_BAD_TEACHER;
+    if (f) atomicOr(err, f);
+    row_ok[r] = bad ? 0 : 1;
+  }
+  if (bad) return;
+  float sum = 0.f;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    val[e] = (key[e] != kNoIndex) ? ex2_approx(val[e] - mx) : 0.f;
+    sum += val[e];
+  }
+  sum = warp_sum(sum);
+  const float inv = 1.0f / sum;
+  const float lgsum = lg2_approx(sum);
+  float pl = 0.f, ps = 0.f, pbest = -1.f;
+  int ibest = kNoIndex;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const float ex = val[e];
+    const float p = ex * inv;
+    if (p > 0.f) pl += p * (lg2_approx(ex) - lgsum) * kLn2;
+    if (key[e] != kNoIndex && (p > pbest || (p == pbest && key[e] < ibest))) {
+      pbest = p;
+      ibest = key[e];
+    }
+    ps += p;
+    val[e] = p;
+  }
+  pl = warp_sum(pl);
+  ps = warp_sum(ps);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float po = __shfl_xor_sync(0xffffffffu, pbest, o);
+    const int io = __shfl_xor_sync(0xffffffffu, ibest, o);
+    if (po > pbest || (po == pbest && io < ibest)) {
+      pbest = po;
+      ibest = io;
+    }
+  }
+  if (lane == 0) {
+    plogp[r] = pl;
+    psum[r] = ps;
+    if (top1 != nullptr) top1[r] = ibest;
+  }
+  // Bitonic sort of (key, p) by key over P2 = 32 E slots, slot g = lane + 32 e.
+#pragma unroll
+  for (int size = 2; size <= 32 * E; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const int g = lane + 32 * e;
+        const int og = g ^ stride;
+        if (stride < 32) {
+          const int ok = __shfl_xor_sync(0xffffffffu, key[e], stride);
+          const float ov = __shfl_xor_sync(0xffffffffu, val[e], stride);
+          const bool up = (g & size) == 0;
+          // the lower slot of the pair keeps the smaller key when ascending
+          const bool keep_small = (g < og) == up;
+          const bool take = keep_small ? (ok < key[e]) : (ok > key[e]);
+          if (take) {
+            key[e] = ok;
+            val[e] = ov;
+          }
+        } else if (og > g) {
+          const int eo = e ^ (stride >> 5);
+          const bool up = (g & size) == 0;
+          if ((key[e] > key[eo]) == up) {
+            const int tk = key[e];
+            key[e] = key[eo];
+            key[eo] = tk;
+            const float tv = val[e];
+            val[e] = val[eo];
+            val[eo] = tv;
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int k = lane + 32 * e;
+    if (k < K) {
+      idx_sorted[r * K + k] = key[e];
+      p_sorted[r * K + k] = (key[e] == kNoIndex) ? 0.f : val[e];
+    }
+  }
+}
+
 // ------------------------------------------------------------- compaction
 // One block: rows[i] = the i-th row with row_ok != 0, n_valid = their count.
 constexpr int kScanThreads = 1024;
@@ -944,6 +1085,21 @@ cudaError_t launch_teacher_prep(const int32_t* idx, const float* logit, const ui
                                 int32_t* top1, uint32_t* err, cudaStream_t s) {
   if (N == 0) return cudaSuccess;
   const int P2 = next_pow2(K < 2 ? 2 : K);
+  if (P2 <= 128) {
+    // one warp per row, the entries in registers
+    const unsigned grid = static_cast<unsigned>(ceil_div(N, kPrepWarpRows));
+    const float k2 = kLog2e / T;
+    if (P2 <= 32)
+      teacher_prep_warp_kernel<1><<<grid, 32 * kPrepWarpRows, 0, s>>>(
+          idx, logit, mask, N, K, V, k2, row_ok, idx_sorted, p_sorted, plogp, psum, top1, err);
+    else if (P2 == 64)
+      teacher_prep_warp_kernel<2><<<grid, 32 * kPrepWarpRows, 0, s>>>(
+          idx, logit, mask, N, K, V, k2, row_ok, idx_sorted, p_sorted, plogp, psum, top1, err);
+    else
+      teacher_prep_warp_kernel<4><<<grid, 32 * kPrepWarpRows, 0, s>>>(
+          idx, logit, mask, N, K, V, k2, row_ok, idx_sorted, p_sorted, plogp, psum, top1, err);
+    return cudaGetLastError();
+  }
   const size_t smem = static_cast<size_t>(P2) * 8;
   cudaError_t e = cudaFuncSetAttribute(teacher_prep_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
