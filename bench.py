@@ -412,7 +412,7 @@ def run_full_teacher(args):
     Ws, Wt = bf(xs.W).to(dev), bf(xt.W).to(dev)
     hs, ht = hs_pin.to(dev), ht_pin.to(dev)
     mask = None if m_pin is None else m_pin.to(dev)
-    chunk = args.chunk or int(kd.load_library().kd_full_kl_default_chunk(N, V))
+    chunk = args.chunk or int(kd.load_library().kd_full_kl_default_chunk(N, d, xt.d, V))
     loss = torch.empty(1, dtype=torch.float32, device=dev)
     gh = torch.empty((N, d), dtype=torch.float32, device=dev)
     gW = torch.empty((V, d), dtype=torch.float32, device=dev)

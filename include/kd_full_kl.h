@@ -49,8 +49,13 @@ extern "C" {
  */
 size_t kd_full_kl_workspace_bytes(int64_t N, int64_t d_s, int64_t d_t, int64_t V, int64_t chunk);
 
-/* The chunk used when a call passes chunk <= 0. */
-int64_t kd_full_kl_default_chunk(int64_t N, int64_t V);
+/*
+ * The chunk used when a call passes chunk <= 0: equal chunks of a multiple of
+ * 128 rows, small enough that both models' exponential tiles stay near 8 GiB
+ * and that both models' hidden states of a chunk (chunk x (d_s + d_t) bf16)
+ * stay within 48 MiB, the part of L2 that holds data re-read by every tile.
+ */
+int64_t kd_full_kl_default_chunk(int64_t N, int64_t d_s, int64_t d_t, int64_t V);
 
 /*
  * Loss, grad_h and grad_W of the full-vocabulary loss.  Per chunk of valid

@@ -110,7 +110,13 @@ size_t kd_topk_kl_workspace_bytes(int64_t N, int64_t d, int64_t V, int32_t K, in
 size_t kd_topk_kl_fwd_workspace_bytes(int64_t N, int64_t d, int64_t V, int32_t K, int64_t chunk,
                                       kd_dtype dtype);
 
-/* The chunk (in tokens) used when a call passes chunk <= 0. */
+/*
+ * The chunk (in tokens) used when a call passes chunk <= 0: equal chunks of a
+ * multiple of 128 tokens, at most 8192, small enough that the chunk's
+ * vocabulary buffer stays near 4 GiB and its hidden states (chunk x d
+ * elements) within 48 MiB, the part of L2 that holds data re-read by every
+ * tile of the chunk's GEMMs.
+ */
 int64_t kd_topk_kl_default_chunk(int64_t N, int64_t d, int64_t V, kd_dtype dtype);
 
 /*

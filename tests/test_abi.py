@@ -63,6 +63,10 @@ def test_workspace_plan_is_linear_in_chunk_not_in_n_times_v(lib):
 
 def test_default_chunk_splits_evenly(lib):
     assert kd.default_chunk(32768, 2880, 201088) == 8192
+    # the chunk's hidden states within 48 MiB of L2: at most 6144 tokens at
+    # d = 4096, made equal (6 chunks of 32K tokens)
+    assert kd.default_chunk(32768, 4096, 151936) == 5504
+    assert kd.default_chunk(32768, 3072, 128256) == 8192
     c = kd.default_chunk(131072, 2880, 201088)
     assert c % 128 == 0 and c * 2 * ((201088 + 255) // 256 * 256) <= 4 << 30
     assert kd.default_chunk(64, 64, 512, kd.KD_FP32) == 128
@@ -158,7 +162,10 @@ def test_full_kl_argument_errors_and_plan(lib):
     assert a < 2 * 8192 * 201216 * 2 * 1.2
     lay = kd.full_kl_workspace_layout(32768, 2880, 2880, 201088, 8192)
     assert lay.chunk == 8192 and lay.off_idx_sorted == 0 and lay.off_rows > 0
-    assert lib.kd_full_kl_default_chunk(32768, 201088) % 128 == 0
+    # both models' hidden states of a chunk within 48 MiB of L2: 4096 tokens
+    # at d_s = d_t = 2880 (8 equal chunks of 32K tokens)
+    assert lib.kd_full_kl_default_chunk(32768, 2880, 2880, 201088) == 4096
+    assert lib.kd_full_kl_default_chunk(1000, 64, 64, 5000) == 1024
 
 
 def test_bounded_wait_test_entry_rejects_bad_arguments(lib):

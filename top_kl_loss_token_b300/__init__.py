@@ -113,7 +113,7 @@ def load_library(path: str = LIB_PATH):
     lib.kd_topk_cache_build.restype = ctypes.c_int
     lib.kd_full_kl_workspace_bytes.argtypes = [i64, i64, i64, i64, i64]
     lib.kd_full_kl_workspace_bytes.restype = sz
-    lib.kd_full_kl_default_chunk.argtypes = [i64, i64]
+    lib.kd_full_kl_default_chunk.argtypes = [i64, i64, i64, i64]
     lib.kd_full_kl_default_chunk.restype = i64
     lib.kd_full_kl_workspace_layout.argtypes = [i64, i64, i64, i64, i64,
                                                 ctypes.POINTER(WorkspaceLayout)]

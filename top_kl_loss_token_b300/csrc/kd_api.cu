@@ -139,7 +139,6 @@ bool encode_tmap_bf16_mn3d(CUtensorMap* m, const void* base, uint64_t inner, uin
 }
 
 int64_t default_chunk(int64_t N, int64_t d, int64_t V, kd_dtype dtype) {
-  (void)d;
   const int64_t elem = dtype == KD_BF16 ? 2 : 4;
   const int64_t ldg = round_up(V, kBN);
   // Keep the per-chunk vocabulary buffer near 4 GiB: a few chunks per call
@@ -151,10 +150,12 @@ int64_t default_chunk(int64_t N, int64_t d, int64_t V, kd_dtype dtype) {
   int64_t cmax = budget / (ldg * elem);
   cmax = cmax / kBM * kBM;
   if (cmax < kBM) cmax = kBM;
-  // Larger chunks were measured slower (8192 vs 11008 tokens: 2.5 % on a
-  // d = 4096 workload, 1.8 % at d = 2880): the chunk's hidden states, re-read
-  // by every tile of both GEMM launches, must stay resident in L2.
+  // The chunk's hidden states must stay resident in L2 (measured at 32K
+  // tokens, d = 4096: chunk 8192 87.3 ms per step, 6144 85.3, 5120 84.6; at
+  // d = 2880, 11008 tokens were 1.8 % slower than 8192).
   if (cmax > kMaxChunk) cmax = kMaxChunk;
+  const int64_t cl2 = l2_chunk_cap(d * elem);
+  if (cmax > cl2) cmax = cl2;
   const int64_t n = N < 1 ? 1 : N;
   const int64_t pieces = ceil_div(n, cmax);
   return round_up(ceil_div(n, pieces), kBM);

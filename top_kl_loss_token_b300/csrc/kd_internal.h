@@ -19,9 +19,19 @@ namespace kd {
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
-// Largest default chunk, in tokens: its hidden states (re-read by every tile
-// of a launch) must stay resident in L2.
+// Largest default chunk, in tokens.
 constexpr int64_t kMaxChunk = 8192;
+// The chunk's hidden states are re-read by every tile of its GEMM launches,
+// so the default chunk keeps them within this many bytes: on B300 about 60 MB
+// of L2 serve re-reads (a buffer re-read by all SMs hits 98 % at 48 MB, 90 %
+// at 64 MB, 25 % at 96 MB), and the streamed operand tiles need the rest.
+constexpr int64_t kChunkL2Bytes = int64_t(48) << 20;
+// Largest multiple of 128 rows (at least 128) whose `row_bytes` per row of
+// hidden states fit in kChunkL2Bytes.
+inline int64_t l2_chunk_cap(int64_t row_bytes) {
+  const int64_t c = kChunkL2Bytes / (row_bytes < 1 ? 1 : row_bytes) / 128 * 128;
+  return c < 128 ? 128 : c;
+}
 // The logsumexp statistics are kept per 128-column block of the vocabulary.
 constexpr int kPB = 128;
 // A sorted-index slot that holds no entry (dropped, or padding).

@@ -114,7 +114,7 @@ constexpr int kStagingBytes = kEpiWarps * kStageWarpBytes;
 
 template <int MODE>
 struct ModeCfg {
-  static constexpr bool kStaged = MODE == kModePass1 || MODE == kModeStore;
+  static constexpr bool kStaged = MODE == kModePass1 || MODE == kModeStore || MODE == kModeDual;
   static constexpr int kStages = kStaged ? kMaxStages - 1 : kMaxStages;
   static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * kStageBytes +
                                   (kStaged ? kStagingBytes : 0) + sizeof(Ctl);
@@ -531,6 +531,34 @@ __device__ __forceinline__ void store_chunk32(float* dst, const float (&v)[32], 
   }
 }
 
+// One 16-byte piece (piece c of 8) of this lane's 128-byte row of a staging
+// buffer, at its place in the 128-byte swizzle layout.
+__device__ __forceinline__ void stage_put(uint8_t* buf, int lane, int c, uint32_t w0, uint32_t w1,
+                                          uint32_t w2, uint32_t w3) {
+  const uint32_t row = smem_u32(buf) + static_cast<uint32_t>(lane) * 128u;
+  st_shared_v4(row + ((static_cast<uint32_t>(c) ^ (static_cast<uint32_t>(lane) & 7u)) << 4), w0,
+               w1, w2, w3);
+}
+
+// Sends the warp's filled staging buffer (32 rows of 128 bytes) to global
+// memory as one box at (x, y), and waits until the buffer may be reused.
+__device__ __forceinline__ void stage_flush(const CUtensorMap* m, uint8_t* buf, int lane, int x,
+                                            int y, bool add) {
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    // streamed outputs: evict-first in L2, so that they leave room for the
+    // operands (measured: pass 1 reads 2.95 instead of 3.44 GB of W per
+    // 8192-token chunk)
+    const uint64_t pol = l2_evict_first_policy();
+    if (add) tma_reduce_add_2d(m, buf, x, y, pol);
+    else tma_store_2d(m, buf, x, y, pol);
+    bulk_commit_group();
+    bulk_wait_group_read0();
+  }
+  __syncwarp();
+}
+
 // Writes one piece of 32 rows x 128 bytes, held one row per lane as 32 words,
 // into the warp's staging buffer in the 128-byte swizzle layout of the
 // output's tensor map, then lane 0 stores it (or adds it) at (x, y) with TMA
@@ -545,19 +573,7 @@ __device__ __forceinline__ void stage_piece(const CUtensorMap* m, uint8_t* buf,
   for (int c = 0; c < 8; ++c)
     st_shared_v4(row + ((static_cast<uint32_t>(c) ^ (static_cast<uint32_t>(lane) & 7u)) << 4),
                  w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-  fence_proxy_async_smem();
-  __syncwarp();
-  if (lane == 0) {
-    // streamed outputs: evict-first in L2, so that they leave room for the
-    // operands (measured: pass 1 reads 2.95 instead of 3.44 GB of W per
-    // 8192-token chunk)
-    const uint64_t pol = l2_evict_first_policy();
-    if (add) tma_reduce_add_2d(m, buf, x, y, pol);
-    else tma_store_2d(m, buf, x, y, pol);
-    bulk_commit_group();
-    bulk_wait_group_read0();
-  }
-  __syncwarp();
+  stage_flush(m, buf, lane, x, y, add);
 }
 
 __device__ __forceinline__ void stage_f32(const CUtensorMap* m, uint8_t* buf, const float (&v)[32],
@@ -929,56 +945,21 @@ __device__ __forceinline__ float max16_tmem(uint32_t ta, int nvalid, float m) {
   return m;
 }
 
-// Exponentials of 16 teacher logits (registers) and 16 student logits (TMEM)
-// relative to the block maxima (base-2 units t2 = z_t k2, s2 = z_s k2), their
-// sums, the teacher-weighted difference sum of 2^(t2 - mt2) (t2 - s2), and
-// both sets stored as bf16 when `store`.
-__device__ __forceinline__ void dual_exp16(const float* t, uint32_t ta_s, int nvalid, float k2,
-                                           float mt2, float ms2, float& lt, float& ls, float& a,
-                                           uint16_t* ut, uint16_t* us, bool store) {
-  float s[16];
-  tmem_ld_x16(ta_s, s);
-  tmem_ld_wait();
-  reg_fence(s);
-#pragma unroll
-  for (int g = 0; g < 2; ++g) {  // 8 columns at a time, stored as they are done
-    uint32_t wt[4], ws[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      float et[2], es[2];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int c = 8 * g + 2 * j + h;
-        const float t2 = t[c] * k2, s2 = s[c] * k2;
-        et[h] = 0.f;
-        es[h] = 0.f;
-        if (c < nvalid) {
-          et[h] = ex2_approx(t2 - mt2);
-          es[h] = ex2_approx(s2 - ms2);
-          lt += et[h];
-          ls += es[h];
-          a = fmaf(et[h], t2 - s2, a);
-        }
-      }
-      wt[j] = pack_bf16x2(et[0], et[1]);
-      ws[j] = pack_bf16x2(es[0], es[1]);
-    }
-    if (store) {
-      reinterpret_cast<uint4*>(ut)[g] = make_uint4(wt[0], wt[1], wt[2], wt[3]);
-      reinterpret_cast<uint4*>(us)[g] = make_uint4(ws[0], ws[1], ws[2], ws[3]);
-    }
-  }
-}
-
 // Full-vocabulary loss epilogue.  The tile's teacher logits are in TMEM
 // columns 0-255 and the student's in 256-511; each thread owns one row and
-// one 128-column block.  It copies its 128 teacher logits into registers and
-// frees the teacher accumulator at once (the next tile's teacher product then
-// runs during the rest of this epilogue), then computes the block maxima
-// m_t, m_s (base 2), the sums l_t, l_s, the cross term a and the stored
-// exponentials of both from the registers and the student accumulator.
+// one 128-column block, each warp 32 rows of it.  In two phases:
+//  1. the warp copies its 128 teacher logits per row into registers and frees
+//     the teacher accumulator at once (the next tile's teacher product then
+//     runs during the rest of this epilogue); it takes the block maximum m_t,
+//     and, while the student product is still running, the exponentials
+//     2^(t2 - m_t) (t2 = z_t k2), their sum l_t, and stores them (bf16) through
+//     the staging buffer, 64 columns per TMA store;
+//  2. once the student product is done: the student's maximum m_s, its
+//     exponentials (sum l_s, stored the same way) and the cross term
+//     a = sum of 2^(t2 - m_t) (t2 - s2), which recomputes the teacher's
+//     exponential rather than keep 128 more values in registers.
 __device__ void epilogue_dual(const KParams& P, const Sizes& S, Ctl* ctl, uint32_t tmem,
-                              const WaitCtx& wc, int warp, int lane, int rank) {
+                              const WaitCtx& wc, int warp, int lane, int rank, uint8_t* wbuf) {
   const int q = warp & 3;
   const int half = (warp - 2) >> 2;
   int slot = 0;
@@ -1002,15 +983,18 @@ __device__ void epilogue_dual(const KParams& P, const Sizes& S, Ctl* ctl, uint32
     const Tile tl = decode_tile<kModeDual>(S, t);
     const uint32_t tp = static_cast<uint32_t>(it) & 1u;
     ++it;
-    const int i = tl.m * kPairM + rank * kBM + q * 32 + lane;
+    const int i0 = tl.m * kPairM + rank * kBM + q * 32;  // the warp's first row
+    const int i = i0 + lane;
     const int col0 = tl.n * kBN + half * 128;
     const int pb = tl.n * 2 + half;
-    const bool live = (i < S.count) && (pb < P.n_pb);
-    const int nv = min(128, P.V - col0);  // warp-uniform
+    const bool block_live = pb < P.n_pb;                  // warp-uniform
+    const bool store = block_live && i0 < S.count;        // warp-uniform: the warp stores
+    const bool live = block_live && i < S.count;          // this row's statistics
+    const int nv = block_live ? min(128, P.V - col0) : 0;  // warp-uniform
     const uint32_t ta = tmem + (static_cast<uint32_t>(q * 32) << 16) +
                         static_cast<uint32_t>(half * 128);
     const uint32_t ts = ta + static_cast<uint32_t>(kBN);
-    // teacher logits -> registers, then free the teacher accumulator
+    // phase 1: teacher logits -> registers, then free the teacher accumulator
     ok = mbar_wait(&ctl->tfull[0], tp, wc);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) break;
@@ -1030,7 +1014,29 @@ __device__ void epilogue_dual(const KParams& P, const Sizes& S, Ctl* ctl, uint32
 #pragma unroll
     for (int j = 0; j < 128; ++j)
       if (j < nv) mt = fmaxf(mt, tv[j]);
-    // student logits: maximum, then exponentials together with the teacher's
+    const float mt2 = mt * k2;
+    float lt = 0.f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {  // 64 columns per stored box
+      if (nv > 64 * h) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {  // 8 columns per 16-byte piece
+          uint32_t w[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int c0 = 64 * h + 8 * c + 2 * j;
+            // the same expression as the cross term's below
+            const float e0 = c0 < nv ? ex2_approx(tv[c0] * k2 - mt2) : 0.f;
+            const float e1 = c0 + 1 < nv ? ex2_approx(tv[c0 + 1] * k2 - mt2) : 0.f;
+            lt += e0 + e1;
+            w[j] = pack_bf16x2(e0, e1);
+          }
+          if (store) stage_put(wbuf, lane, c, w[0], w[1], w[2], w[3]);
+        }
+        if (store) stage_flush(&P.tmOut[1], wbuf, lane, col0 + 64 * h, i0, false);
+      }
+    }
+    // phase 2: student logits: maximum, then exponentials and the cross term
     ok = mbar_wait(&ctl->tfull[1], tp, wc);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) break;
@@ -1039,18 +1045,49 @@ __device__ void epilogue_dual(const KParams& P, const Sizes& S, Ctl* ctl, uint32
 #pragma unroll
     for (int c = 0; c < 8; ++c)
       if (nv > 16 * c) ms = max16_tmem(ts + 16 * c, nv - 16 * c, ms);
-    const float mt2 = mt * k2, ms2 = ms * k2;
-    float lt = 0.f, ls = 0.f, a = 0.f;
-    const int64_t urow = static_cast<int64_t>(live ? i : 0) * P.ldg + col0;
-    uint16_t* ut = P.u_t + urow;
-    uint16_t* us = P.u + urow;
-    // every lane takes part in the (warp-collective) TMEM loads; only rows of
-    // the chunk store
+    const float ms2 = ms * k2;
+    float ls = 0.f, a = 0.f;
+    // every lane takes part in the (warp-collective) TMEM loads
 #pragma unroll
-    for (int c = 0; c < 8; ++c)
-      if (nv > 16 * c)
-        dual_exp16(tv + 16 * c, ts + 16 * c, nv - 16 * c, k2, mt2, ms2, lt, ls, a, ut + 16 * c,
-                   us + 16 * c, live);
+    for (int h = 0; h < 2; ++h) {
+      if (nv > 64 * h) {
+#pragma unroll
+        for (int c16 = 0; c16 < 4; ++c16) {
+          const int cb = 64 * h + 16 * c16;  // first column of these 16
+          float sv[16];
+          if (nv > cb) {
+            tmem_ld_x16(ts + cb, sv);
+            tmem_ld_wait();
+            reg_fence(sv);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) sv[j] = 0.f;
+          }
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              float es[2];
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int c = cb + 8 * g + 2 * j + e;
+                es[e] = 0.f;
+                if (c < nv) {
+                  const float t2 = tv[c] * k2, s2 = sv[8 * g + 2 * j + e] * k2;
+                  es[e] = ex2_approx(s2 - ms2);
+                  ls += es[e];
+                  a = fmaf(ex2_approx(t2 - mt2), t2 - s2, a);
+                }
+              }
+              w[j] = pack_bf16x2(es[0], es[1]);
+            }
+            if (store) stage_put(wbuf, lane, 2 * c16 + g, w[0], w[1], w[2], w[3]);
+          }
+        }
+        if (store) stage_flush(&P.tmOut[0], wbuf, lane, col0 + 64 * h, i0, false);
+      }
+    }
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive_cluster(tempty1);
@@ -1063,6 +1100,9 @@ __device__ void epilogue_dual(const KParams& P, const Sizes& S, Ctl* ctl, uint32
       P.part_l[o] = ls;
     }
   }
+  // every staged store complete before the kernel ends
+  if (lane == 0) bulk_wait_group0();
+  __syncwarp();
 }
 
 template <int MODE>
@@ -1130,7 +1170,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     else if (MODE == kModeStore)
       epilogue_store(P, S, ctl, tmem, wc, warp, lane, static_cast<int>(rank), wbuf);
     else if (MODE == kModeDual)
-      epilogue_dual(P, S, ctl, tmem, wc, warp, lane, static_cast<int>(rank));
+      epilogue_dual(P, S, ctl, tmem, wc, warp, lane, static_cast<int>(rank), wbuf);
     else
       epilogue_topk<MODE>(P, S, ctl, tmem, wc, warp, lane, static_cast<int>(rank));
   }
@@ -1351,6 +1391,11 @@ cudaError_t launch_tc_dual_pass1(const DualPass1Args& p, const ChunkArgs& a, cud
   P.u = p.u_s;
   P.ldg = a.ldg;
   P.u_t = p.u_t;
+  // both exponential tiles leave through the staging buffers: student in
+  // tmOut[0], teacher in tmOut[1]
+  if (!encode_tmap_store(&P.tmOut[0], p.u_s, false, a.ldg, a.cpad, a.ldg, 64, 32) ||
+      !encode_tmap_store(&P.tmOut[1], p.u_t, false, a.ldg, a.cpad, a.ldg, 64, 32))
+    return cudaErrorInvalidValue;
   P.part_mt = p.part_mt;
   P.part_lt = p.part_lt;
   P.part_a = p.part_a;
