@@ -10,6 +10,7 @@
 // loss, form the gradient of the loss with respect to the logits one chunk at
 // a time, and reduce the loss.  Every exponential is taken in base 2:
 // s2 = z * log2(e) / T, so softmax(z / T) = 2^(s2 - lse2).
+#include <limits.h>
 #include <math.h>
 #include <stdint.h>
 
@@ -493,10 +494,16 @@ __global__ void __launch_bounds__(kBoffRows * kBoffGroups) bucket_offsets_kernel
     if (__ldg(lst + mid) < target0) lo = mid + 1;
     else hi = mid;
   }
+  // the next entry's index stays in a register: most blocks hold no entry,
+  // so the loop is a compare and a store per block
   int off = lo;
+  int nxt = off < a.K ? __ldg(lst + off) : INT_MAX;
   for (int pb = pb0; pb < pb1; ++pb) {
     const int target = pb * kPB;
-    while (off < a.K && __ldg(lst + off) < target) ++off;
+    while (nxt < target) {
+      ++off;
+      nxt = off < a.K ? __ldg(lst + off) : INT_MAX;
+    }
     a.boff[static_cast<int64_t>(pb) * a.cpad + i] = static_cast<uint16_t>(off);
   }
 }
@@ -524,7 +531,29 @@ __global__ void __launch_bounds__(kLseRows * kLseGroups) lse_kernel(
   const bool live = i < count;
   float M = -INFINITY, L = 0.f, PS = 0.f;
   if (live) {
-    for (int pb = y; pb < a.n_pb; pb += kLseGroups) {
+    // four blocks' statistics loaded before they are combined, so that
+    // several loads per thread are in flight
+    int pb = y;
+    for (; pb + 3 * kLseGroups < a.n_pb; pb += 4 * kLseGroups) {
+      float m[4], l[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t o = static_cast<int64_t>(pb + u * kLseGroups) * a.cpad + i;
+        m[u] = a.part_m[o];
+        l[u] = a.part_l[o];
+        PS += a.part_ps[o];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (m[u] > M) {
+          L = L * ex2_approx(M - m[u]) + l[u];
+          M = m[u];
+        } else {
+          L += l[u] * ex2_approx(m[u] - M);
+        }
+      }
+    }
+    for (; pb < a.n_pb; pb += kLseGroups) {
       const int64_t o = static_cast<int64_t>(pb) * a.cpad + i;
       const float m = a.part_m[o], l = a.part_l[o];
       PS += a.part_ps[o];
