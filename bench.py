@@ -397,12 +397,7 @@ def run_full_teacher(args):
         if c.get("mask") == "packed":
             c["mask_frac_range"] = None
     xs = synth.make_inputs(**c)
-    ct = dict(c)
-    ct["seed"] = c["seed"] + 50
-    ct["mask"] = None
-    ct.pop("mask_frac_range", None)
-    ct["K"] = 1
-    xt = synth.make_inputs(**ct)
+    xt = synth.make_inputs(**synth.full_teacher_config(c))
     N, d, V = xs.N, xs.d, xs.V
 
     def bf(a):

@@ -38,7 +38,8 @@ def _log_softmax(x):
 
 def full_kl_fwd_bwd(h_s, W_s, h_t, W_t, mask, T, block_rows=256, want_grads=True):
     """Returns dict(loss, grad_h [N, d_s], grad_W [V, d_s], loss_rows [N],
-    lse_s [N] (logsumexp of s), valid [N] bool, n_valid)."""
+    lse_s [N] (logsumexp of s), lse_t [N] (logsumexp of t), valid [N] bool,
+    n_valid)."""
     h_s = np.asarray(h_s, dtype=np.float64)
     W_s = np.asarray(W_s, dtype=np.float64)
     h_t = np.asarray(h_t, dtype=np.float64)
@@ -49,6 +50,7 @@ def full_kl_fwd_bwd(h_s, W_s, h_t, W_t, mask, T, block_rows=256, want_grads=True
     n_valid = int(valid.sum())
     loss_rows = np.zeros(N)
     lse_s = np.zeros(N)
+    lse_t = np.zeros(N)
     grad_h = np.zeros_like(h_s) if want_grads else None
     grad_W = np.zeros_like(W_s) if want_grads else None
     for r0 in range(0, N, block_rows):
@@ -64,13 +66,15 @@ def full_kl_fwd_bwd(h_s, W_s, h_t, W_t, mask, T, block_rows=256, want_grads=True
         loss_rows[rows] = (p * (logp - logq)).sum(axis=1)
         smax = s.max(axis=1)
         lse_s[rows] = smax + np.log(np.exp(s - smax[:, None]).sum(axis=1))
+        tmax = t.max(axis=1)
+        lse_t[rows] = tmax + np.log(np.exp(t - tmax[:, None]).sum(axis=1))
         if want_grads:
             G = (np.exp(logq) - p) / (T * n_valid)
             grad_h[rows] = G @ W_s
             grad_W += G.T @ h_s[rows]
     loss = float(loss_rows[valid].sum() / n_valid) if n_valid > 0 else 0.0
     return dict(loss=loss, grad_h=grad_h, grad_W=grad_W, loss_rows=loss_rows, lse_s=lse_s,
-                valid=valid, n_valid=n_valid)
+                lse_t=lse_t, valid=valid, n_valid=n_valid)
 
 
 def full_kl_grad_logits(h_s, W_s, h_t, W_t, mask, T):
@@ -122,3 +126,32 @@ def full_kl_sampled_rows(h_s, W_s, h_t, W_t, mask, T, rows):
     grad_h[~v] = 0.0
     loss_rows[~v] = 0.0
     return dict(loss_rows=loss_rows, lse_s=lse_s, grad_h=grad_h, valid=v, n_valid=n_valid)
+
+
+def full_kl_grad_W_rows(h_s, W_s, h_t, W_t, mask, T, vocab_rows, lse_s, lse_t,
+                        block_rows=4096):
+    """Rows vocab_rows of grad_W = (dL/dz_s)^T h_s, given every row's lse_s and
+    lse_t (from full_kl_fwd_bwd): column v of dL/dz_s is
+    (exp(s_v - lse_s) - exp(t_v - lse_t)) / (T N_valid) over the valid rows,
+    so only those columns of both products are formed."""
+    h_s = np.asarray(h_s, dtype=np.float64)
+    h_t = np.asarray(h_t, dtype=np.float64)
+    vr = np.asarray(vocab_rows)
+    Ws = np.asarray(W_s, dtype=np.float64)[vr]
+    Wt = np.asarray(W_t, dtype=np.float64)[vr]
+    N = h_s.shape[0]
+    valid = np.ones(N, dtype=bool) if mask is None else np.asarray(mask) != 0
+    n_valid = int(valid.sum())
+    out = np.zeros((vr.size, h_s.shape[1]))
+    if n_valid == 0:
+        return out
+    for r0 in range(0, N, block_rows):
+        rows = np.arange(r0, min(N, r0 + block_rows))
+        rows = rows[valid[rows]]
+        if rows.size == 0:
+            continue
+        s = (h_s[rows] @ Ws.T) / T
+        t = (h_t[rows] @ Wt.T) / T
+        G = (np.exp(s - lse_s[rows, None]) - np.exp(t - lse_t[rows, None])) / (T * n_valid)
+        out += G.T @ h_s[rows]
+    return out

@@ -14,10 +14,15 @@ Every value stored here comes from oracle/ and the seeded input generator
   * about 200 rows of grad_W (half the vocabulary rows of teacher entries of
     rank 1, half uniform, plus the first and the last row), each computed from
     the oracle's own lse.
+For the full-vocabulary loss on config 3's sizes (student = config 3, teacher
+drawn by synth.full_teacher_config, as the benchmark's --full-teacher mode
+does): the whole-batch loss, every token's lse (of the student logits) and
+loss term, and about 200 grad_W rows (uniform vocabulary rows plus the first
+and the last), from oracle/full_kl_oracle.py.
 Each file carries a digest of the inputs it was computed from; a test that
 finds a different digest recomputes.
 
-    python tests/golden/make_fullsize_oracle.py [config ...]     (default: 3 5 4)
+    python tests/golden/make_fullsize_oracle.py [config ...]  (default: 3 5 4 full3)
 """
 import hashlib
 import os
@@ -93,10 +98,68 @@ def load_or_compute(cfg: int, x, log=None):
     return res
 
 
+def full_vocab_sample(xs, n_uniform=200) -> np.ndarray:
+    """Vocabulary rows of grad_W checked for the full-vocabulary loss."""
+    rng = np.random.default_rng(2000 + xs.seed)
+    return np.unique(np.concatenate([rng.integers(0, xs.V, size=n_uniform), [0, xs.V - 1]]))
+
+
+def full_cache_path(cfg: int) -> str:
+    return os.path.join(CACHE_DIR, f"full_kl_config{cfg}.npz")
+
+
+def compute_full(xs, xt, block_rows=256, log=None):
+    """The full-vocabulary oracle's whole-batch forward and sampled grad_W
+    rows for student xs and teacher xt."""
+    import oracle
+    t0 = time.time()
+    hs, Ws, ht, Wt = xs.h_f32(), xs.W_f32(), xt.h_f32(), xt.W_f32()
+    full = oracle.full_kl_fwd_bwd(hs, Ws, ht, Wt, xs.mask, xs.T, block_rows=block_rows,
+                                  want_grads=False)
+    t1 = time.time()
+    vr = full_vocab_sample(xs)
+    gW = oracle.full_kl_grad_W_rows(hs, Ws, ht, Wt, xs.mask, xs.T, vr, full["lse_s"],
+                                    full["lse_t"])
+    t2 = time.time()
+    if log is not None:
+        log(f"full-vocabulary {xs.name}: forward {t1 - t0:.0f} s, {vr.size} grad_W rows "
+            f"{t2 - t1:.0f} s")
+    return dict(digest=np.array(input_digest(xs) + input_digest(xt)),
+                loss=np.float64(full["loss"]), n_valid=np.int64(full["n_valid"]),
+                lse=full["lse_s"], loss_rows=full["loss_rows"], vocab_rows=vr, grad_W_rows=gW)
+
+
+def load_or_compute_full(cfg: int, xs, xt, log=None):
+    """The cached full-vocabulary oracle results for config cfg if they match
+    the inputs, else computed now (and cached)."""
+    path = full_cache_path(cfg)
+    dig = input_digest(xs) + input_digest(xt)
+    if os.path.exists(path):
+        with np.load(path) as z:
+            if str(z["digest"]) == dig:
+                return {k: z[k] for k in z.files}
+    res = compute_full(xs, xt, log=log)
+    os.makedirs(CACHE_DIR, exist_ok=True)
+    tmp = path + f".tmp{os.getpid()}.npz"
+    np.savez(tmp, **res)
+    os.replace(tmp, path)
+    return res
+
+
 def main(argv):
     from top_kl_loss_token_b300 import synth
-    cfgs = [int(a) for a in argv] or [3, 5, 4]
-    for cfg in cfgs:
+    args = list(argv) or ["3", "5", "4", "full3"]
+    for a in args:
+        if a.startswith("full"):
+            cfg = int(a[4:])
+            xs, xt = synth.make_full_teacher_pair(cfg)
+            res = load_or_compute_full(cfg, xs, xt, log=lambda s: print(s, flush=True))
+            print(f"full-vocabulary config {cfg}: loss {float(res['loss']):.9f}, N_valid "
+                  f"{int(res['n_valid'])}, {res['vocab_rows'].size} grad_W rows -> "
+                  f"{full_cache_path(cfg)}", flush=True)
+            del xs, xt, res
+            continue
+        cfg = int(a)
         x = synth.make_config(cfg)
         res = load_or_compute(cfg, x, log=lambda s: print(s, flush=True))
         print(f"config {cfg}: loss {float(res['loss']):.9f}, N_valid {int(res['n_valid'])}, "

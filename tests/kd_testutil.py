@@ -26,6 +26,17 @@ def fullsize_oracle(cfg, x):
     return mod.load_or_compute(cfg, x)
 
 
+def fullsize_full_oracle(cfg, xs, xt):
+    """The full-vocabulary oracle's whole-batch forward and sampled grad_W rows
+    for student xs and teacher xt (config cfg's sizes), from the same local
+    cache (computed now, and cached, when missing or made from other inputs)."""
+    spec = importlib.util.spec_from_file_location(
+        "make_fullsize_oracle", os.path.join(_HERE, "golden", "make_fullsize_oracle.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod.load_or_compute_full(cfg, xs, xt)
+
+
 def to_device(x, device="cuda"):
     import torch
     if x.dtype == "bf16":

@@ -140,6 +140,29 @@ def test_sampled_rows_match_the_full_computation():
     np.testing.assert_allclose(s["lse_s"][v], r["lse_s"][rows][v], rtol=1e-12)
 
 
+def test_sampled_grad_W_rows_are_autograd_of_kl_div():
+    # the column-sampled grad_W (used at full size, where the dense one is out
+    # of reach) against torch autograd of F.kl_div, and the per-row logsumexps
+    # it takes against torch.logsumexp
+    hs, Ws, ht, Wt = _inputs(11, N=20, V=50)
+    mask = np.ones(20, np.uint8)
+    mask[[3, 4, 17]] = 0
+    T = 2.0
+    r = fko.full_kl_fwd_bwd(hs, Ws, ht, Wt, mask, T, block_rows=7)
+    v = mask != 0
+    np.testing.assert_allclose(r["lse_t"][v], torch.logsumexp(torch.tensor(ht @ Wt.T) / T,
+                                                              dim=1).numpy()[v], rtol=1e-13)
+    np.testing.assert_allclose(r["lse_s"][v], torch.logsumexp(torch.tensor(hs @ Ws.T) / T,
+                                                              dim=1).numpy()[v], rtol=1e-13)
+    rows = torch.from_numpy(np.nonzero(mask)[0])
+    tWs = torch.tensor(Ws, requires_grad=True)
+    _torch_loss(torch.tensor(hs), tWs, torch.tensor(ht), torch.tensor(Wt), T, rows).backward()
+    vr = np.array([0, 7, 8, 31, 49])
+    got = fko.full_kl_grad_W_rows(hs, Ws, ht, Wt, mask, T, vr, r["lse_s"], r["lse_t"],
+                                  block_rows=6)
+    np.testing.assert_allclose(got, tWs.grad.numpy()[vr], rtol=1e-10, atol=1e-15)
+
+
 # ------------------------------------------------------------ planted mistakes
 
 PINS = [lambda: test_kl_div_batchmean_and_its_autograd(2.0), test_zero_when_student_equals_teacher,

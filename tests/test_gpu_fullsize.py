@@ -18,7 +18,7 @@ import pytest
 
 import oracle
 from top_kl_loss_token_b300 import synth
-from kd_testutil import TOL, fullsize_oracle, max_rel_err, run_gpu, to_device
+from kd_testutil import TOL, fullsize_full_oracle, fullsize_oracle, max_rel_err, run_gpu, to_device
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -78,7 +78,7 @@ def check_grad_W_rows(x, got, full):
     assert max_rel_err(got["grad_W"][vr], full["grad_W_rows"]) <= tg
 
 
-def check_sum_rule(x, got):
+def check_sum_rule(x, got, rounding=3.01):
     """Every column of grad_W sums to ~0.
 
     Exactly, sum_v dL/dz_rv = (sum_v q_rv - sum_k p_rk) / (T N_valid) = 0.  The
@@ -91,13 +91,16 @@ def check_sum_rule(x, got):
     fp32 logsumexp and teacher sums (a per-token offset, not zero-mean) and
     1e-5 of sum_v |grad_W_vj| for the fp32 accumulation.  Dropping the
     teacher term would give |sum_r h_rj| / (T N_valid), about 20 times the
-    bound."""
+    bound.  The full-vocabulary loss stores G~ = bf16(alpha_s u~_s - alpha_t
+    u~_t) with both exponentials rounded once: 2^-9 (q + p) from them and
+    2^-9 (q + p) from the tile, so e = 4.01 * 2^-9 / (T N_valid) there
+    (`rounding`)."""
     gW = got["grad_W"]
     h = x.h_f32().astype(np.float64)
     valid = np.ones(x.N, bool) if x.mask is None else x.mask != 0
     hv = h[valid]
     tn = x.T * got["n_valid"]
-    e = 3.01 * 2.0 ** -9 / tn
+    e = rounding * 2.0 ** -9 / tn
     bound = (8.0 * e * np.sqrt((hv * hv).sum(axis=0)) + 1e-5 * np.abs(hv).sum(axis=0) / tn
              + 1e-5 * np.abs(gW).sum(axis=0))
     colsum = gW.sum(axis=0)
@@ -224,3 +227,42 @@ def test_full_size_forward_only_matches_fwd_bwd(kd):
     assert b["loss"] == pytest.approx(a["loss"], rel=1e-6)
     np.testing.assert_array_equal(b["rows"], a["rows"])
     np.testing.assert_allclose(b["lse"], a["lse"], rtol=1e-6)
+
+
+def test_full_vocabulary_loss_at_full_size(kd):
+    """The full-vocabulary loss (kd_full_kl_fwd_bwd) on config 3's sizes in
+    the launch configuration `bench.py --full-teacher` times: 32K tokens,
+    d_s = d_t = 2880, V = 201,088, the default 4096-token chunk (8 chunks,
+    grad_W accumulated over them).  Against the full-vocabulary oracle: the
+    whole-batch loss, every token's lse and loss term, sampled grad_h and
+    grad_W rows; the sum rule and the projection identity on all of grad_W."""
+    import torch
+    xs, xt = synth.make_full_teacher_pair(3)
+    full = fullsize_full_oracle(3, xs, xt)
+    hs, Ws, _, _, mask = to_device(xs)
+    ht, Wt = to_device(xt)[:2]
+    N, d, V = xs.N, xs.d, xs.V
+    err = torch.zeros(1, dtype=torch.int32, device=hs.device)
+    loss, gh, gW, ws = kd.full_kl_fwd_bwd(hs, Ws, ht, Wt, mask, xs.T, 0, err_flags=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    lay = kd.full_kl_workspace_layout(N, d, xt.d, V, 0)
+    assert int(lay.chunk) == 4096
+    ctrl = ws[lay.off_ctrl: lay.off_ctrl + 16].cpu().numpy()
+    nv = int(ctrl[4:8].view(np.int32)[0])
+    got = dict(loss=float(loss.item()), n_valid=nv,
+               grad_h=gh.cpu().numpy().astype(np.float64),
+               grad_W=gW.cpu().numpy().astype(np.float64),
+               rows=kd.workspace_view(ws, lay, "rows", N, torch.int32)[:nv].cpu().numpy(),
+               lse=kd.workspace_view(ws, lay, "lse", N, torch.float32)[:nv].cpu().numpy(),
+               loss_rows=kd.workspace_view(ws, lay, "loss_rows", N,
+                                           torch.float32)[:nv].cpu().numpy())
+    del gh, gW, ws
+    check_whole_batch(xs, got, full)
+    check_grad_W_rows(xs, got, full)
+    rows = sample_rows(xs, n=64)
+    ref = oracle.full_kl_sampled_rows(xs.h_f32(), xs.W_f32(), xt.h_f32(), xt.W_f32(), xs.mask,
+                                      xs.T, rows)
+    assert max_rel_err(got["grad_h"][rows], ref["grad_h"]) <= TOL["bf16"][1]
+    check_sum_rule(xs, got, rounding=4.01)
+    check_projection_identity(xs, got)

@@ -218,3 +218,24 @@ def make_config(i: int, **overrides) -> KDInputs:
     c = dict(CONFIGS[i])
     c.update(overrides)
     return make_inputs(**c)
+
+
+def full_teacher_config(c: dict) -> dict:
+    """The teacher of a full-vocabulary workload built from the student's
+    recipe c: the same sizes (so d_t = d_s), its own seed, no mask; its top-K
+    fields are unused (K = 1)."""
+    ct = dict(c)
+    ct["seed"] = c["seed"] + 50
+    ct["mask"] = None
+    ct.pop("mask_frac_range", None)
+    ct["K"] = 1
+    return ct
+
+
+def make_full_teacher_pair(i: int, **overrides):
+    """(student, teacher) inputs of the full-vocabulary workload on config i:
+    the student is config i (with the overrides), the teacher
+    full_teacher_config of it; both models' h and W are used."""
+    c = dict(CONFIGS[i])
+    c.update(overrides)
+    return make_inputs(**c), make_inputs(**full_teacher_config(c))
