@@ -824,7 +824,26 @@ __global__ void __launch_bounds__(kLseRows * kLseGroups) lse_dual_kernel(
   const bool live = i < count;
   float Mt = -INFINITY, Lt = 0.f, At = 0.f, Ms = -INFINITY, Ls = 0.f, dummy = 0.f;
   if (live) {
-    for (int pb = y; pb < a.n_pb; pb += kLseGroups) {
+    // four blocks' statistics loaded before they are merged (same order)
+    int pb = y;
+    for (; pb + 3 * kLseGroups < a.n_pb; pb += 4 * kLseGroups) {
+      float mt[4], lt[4], at[4], ms[4], ls[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t o = static_cast<int64_t>(pb + u * kLseGroups) * a.cpad + i;
+        mt[u] = part_mt[o];
+        lt[u] = part_lt[o];
+        at[u] = part_a[o];
+        ms[u] = a.part_m[o];
+        ls[u] = a.part_l[o];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        merge_block(mt[u], lt[u], at[u], Mt, Lt, At);
+        merge_block(ms[u], ls[u], 0.f, Ms, Ls, dummy);
+      }
+    }
+    for (; pb < a.n_pb; pb += kLseGroups) {
       const int64_t o = static_cast<int64_t>(pb) * a.cpad + i;
       merge_block(part_mt[o], part_lt[o], part_a[o], Mt, Lt, At);
       merge_block(a.part_m[o], a.part_l[o], 0.f, Ms, Ls, dummy);
@@ -854,7 +873,23 @@ __global__ void __launch_bounds__(kLseRows * kLseGroups) lse_dual_kernel(
   if (!live) return;
   const float lse2_t = sLseT[x], lse2_s = sLseS[x];
   const float scale = grad_scale(a.n_norm, T);
-  for (int pb = y; pb < a.n_pb; pb += kLseGroups) {
+  int pb = y;
+  for (; pb + 3 * kLseGroups < a.n_pb; pb += 4 * kLseGroups) {
+    float ms[4], mt[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t o = static_cast<int64_t>(pb + u * kLseGroups) * a.cpad + i;
+      ms[u] = a.part_m[o];
+      mt[u] = part_mt[o];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t o = static_cast<int64_t>(pb + u * kLseGroups) * a.cpad + i;
+      a.part_m[o] = ex2_approx(ms[u] - lse2_s) * scale;
+      part_mt[o] = ex2_approx(mt[u] - lse2_t) * scale;
+    }
+  }
+  for (; pb < a.n_pb; pb += kLseGroups) {
     const int64_t o = static_cast<int64_t>(pb) * a.cpad + i;
     a.part_m[o] = ex2_approx(a.part_m[o] - lse2_s) * scale;
     part_mt[o] = ex2_approx(part_mt[o] - lse2_t) * scale;
