@@ -100,28 +100,34 @@ def full_kl_grad_logits(h_s, W_s, h_t, W_t, mask, T):
     return dict(G=G, q=q, p=p, valid=valid, n_valid=n_valid)
 
 
-def full_kl_sampled_rows(h_s, W_s, h_t, W_t, mask, T, rows):
+def full_kl_sampled_rows(h_s, W_s, h_t, W_t, mask, T, rows, block_rows=64):
     """Per-row results of the full loss for the given rows only: loss_rows,
     lse_s and grad_h rows, with N_valid over the whole batch.  Masked rows
-    give a zero loss term and a zero grad_h row, as in full_kl_fwd_bwd."""
+    give a zero loss term and a zero grad_h row, as in full_kl_fwd_bwd.  The
+    rows are taken block_rows at a time."""
     valid = (np.ones(np.asarray(h_s).shape[0], dtype=bool) if mask is None
              else np.asarray(mask) != 0)
     n_valid = int(valid.sum())
     rows = np.asarray(rows)
-    hs = np.asarray(h_s, dtype=np.float64)[rows]
-    ht = np.asarray(h_t, dtype=np.float64)[rows]
     Ws = np.asarray(W_s, dtype=np.float64)
     Wt = np.asarray(W_t, dtype=np.float64)
-    t = (ht @ Wt.T) / T
-    s = (hs @ Ws.T) / T
-    logp = _log_softmax(t)
-    logq = _log_softmax(s)
-    p = np.exp(logp)
-    loss_rows = (p * (logp - logq)).sum(axis=1)
-    smax = s.max(axis=1)
-    lse_s = smax + np.log(np.exp(s - smax[:, None]).sum(axis=1))
-    G = (np.exp(logq) - p) / (T * max(n_valid, 1))
-    grad_h = G @ Ws
+    loss_rows = np.zeros(rows.size)
+    lse_s = np.zeros(rows.size)
+    grad_h = np.zeros((rows.size, Ws.shape[1]))
+    for b0 in range(0, rows.size, block_rows):
+        rr = rows[b0:b0 + block_rows]
+        hs = np.asarray(h_s, dtype=np.float64)[rr]
+        ht = np.asarray(h_t, dtype=np.float64)[rr]
+        t = (ht @ Wt.T) / T
+        s = (hs @ Ws.T) / T
+        logp = _log_softmax(t)
+        logq = _log_softmax(s)
+        p = np.exp(logp)
+        loss_rows[b0:b0 + rr.size] = (p * (logp - logq)).sum(axis=1)
+        smax = s.max(axis=1)
+        lse_s[b0:b0 + rr.size] = smax + np.log(np.exp(s - smax[:, None]).sum(axis=1))
+        G = (np.exp(logq) - p) / (T * max(n_valid, 1))
+        grad_h[b0:b0 + rr.size] = G @ Ws
     v = valid[rows]
     grad_h[~v] = 0.0
     loss_rows[~v] = 0.0
