@@ -745,20 +745,27 @@ __global__ void __launch_bounds__(kPrepGradThreads) grad_prepare_kernel(
     }
     __syncthreads();
   }
-  if (tid < 32) {
+  {
     // Teacher entries: u[i, v] -= p_v * beta_row, so that alpha_row * u becomes
     // (softmax - p) / (T n).  The sorted list keeps equal indices together:
-    // each run is summed first and applied once, by the lane that owns its
-    // first entry (distinct runs touch distinct columns).
+    // each run is summed first and applied once, by the thread that owns its
+    // first entry (distinct runs touch distinct columns).  One entry per
+    // thread: its index, its neighbours' and its probability are loaded
+    // together, so only the read of u waits on them.
     const float br = a.beta_row[i];
     const int64_t r = a.rows[a.row0 + i];
     const int32_t* lidx = a.idx_sorted + r * a.K;
     const float* lp = a.p_sorted + r * a.K;
-    for (int e = tid; e < a.K; e += 32) {
+    for (int e = tid; e < a.K; e += kPrepGradThreads) {
       const int v = __ldg(lidx + e);
-      if (v == kNoIndex || (e > 0 && __ldg(lidx + e - 1) == v)) continue;
+      const int vp = e > 0 ? __ldg(lidx + e - 1) : -1;
+      const int vn = e + 1 < a.K ? __ldg(lidx + e + 1) : -1;
       float ps = __ldg(lp + e);
-      for (int f = e + 1; f < a.K && __ldg(lidx + f) == v; ++f) ps += __ldg(lp + f);
+      if (v == kNoIndex || vp == v) continue;
+      if (vn == v) {
+        ps += __ldg(lp + e + 1);
+        for (int f = e + 2; f < a.K && __ldg(lidx + f) == v; ++f) ps += __ldg(lp + f);
+      }
       uint16_t* at = row + v;
       const float x = __uint_as_float(static_cast<uint32_t>(*at) << 16);
       *at = static_cast<uint16_t>(pack_bf16x2(fmaf(-ps, br, x), 0.f) & 0xFFFFu);
