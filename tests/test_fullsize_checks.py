@@ -102,3 +102,47 @@ def test_projection_identity_catches_a_missing_tile(problem, scaled):
     bad["grad_h"][1024:1152] = 0.0
     with pytest.raises(AssertionError):
         check_projection_identity(x, bad, alpha)
+
+
+# ------------------------------------------------- the full-vocabulary loss
+
+@pytest.fixture(scope="module")
+def full_problem():
+    xs, xt = synth.make_full_teacher_pair(2, N=2048, d=64, V=3000, T=2.0, mask="random0.1",
+                                          seed=41)
+    g = oracle.full_kl_grad_logits(xs.h_f32(), xs.W_f32(), xt.h_f32(), xt.W_f32(), xs.mask,
+                                   xs.T)
+    tn = xs.T * g["n_valid"]
+    # the tile as the GPU builds it: both stored exponentials rounded to bf16
+    # (a power-of-two block reference does not change their rounding), the
+    # per-block factors applied, the difference rounded to bf16 once more
+    Gq = _bf16((_bf16(g["q"]) - _bf16(g["p"])) / tn)
+    return xs, g, Gq
+
+
+def test_full_vocabulary_checks_pass_on_rounded_results(full_problem):
+    xs, g, Gq = full_problem
+    exact = _outputs(xs, g["G"], g["n_valid"])
+    assert check_sum_rule(xs, exact, rounding=4.01) < 0.05
+    assert check_projection_identity(xs, exact) < 1e-12
+    rounded = _outputs(xs, Gq, g["n_valid"])
+    assert check_sum_rule(xs, rounded, rounding=4.01) <= 1.0
+    check_projection_identity(xs, rounded)
+
+
+def test_full_vocabulary_checks_catch_planted_mistakes(full_problem):
+    xs, g, Gq = full_problem
+    tn = xs.T * g["n_valid"]
+    # the teacher's distribution left out of dL/dz_s
+    with pytest.raises(AssertionError):
+        check_sum_rule(xs, _outputs(xs, _bf16(g["q"] / tn), g["n_valid"]), rounding=4.01)
+    # the teacher term without its temperature
+    with pytest.raises(AssertionError):
+        check_sum_rule(xs, _outputs(xs, _bf16(g["q"] / tn - g["p"] / g["n_valid"]),
+                                    g["n_valid"]), rounding=4.01)
+    out = _outputs(xs, Gq, g["n_valid"])
+    bad = dict(out)
+    bad["grad_W"] = out["grad_W"].copy()
+    bad["grad_W"][512:768] = 0.0
+    with pytest.raises(AssertionError):
+        check_projection_identity(xs, bad)
