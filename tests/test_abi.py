@@ -5,6 +5,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 import top_kl_loss_token_b300 as kd
@@ -70,6 +71,32 @@ def test_default_chunk_splits_evenly(lib):
     c = kd.default_chunk(131072, 2880, 201088)
     assert c % 128 == 0 and c * 2 * ((201088 + 255) // 256 * 256) <= 4 << 30
     assert kd.default_chunk(64, 64, 512, kd.KD_FP32) == 128
+
+
+def test_default_chunk_rule_over_many_sizes(lib):
+    # the rule kd_topk_kl.h and kd_full_kl.h state: equal chunks of a multiple
+    # of 128 rows, at most 8192, the vocabulary buffers within their budget,
+    # and the chunk's hidden states within 48 MiB (unless one 128-row chunk is
+    # already more)
+    rng = np.random.default_rng(0)
+    l2 = 48 << 20
+    for _ in range(300):
+        N = int(rng.integers(1, 300000))
+        d = int(rng.integers(1, 1024)) * 8
+        V = int(rng.integers(1, 400000))
+        ldg = -(-V // 256) * 256
+        for dt, elem in ((kd.KD_BF16, 2), (kd.KD_FP32, 4)):
+            c = kd.default_chunk(N, d, V, dt)
+            assert c % 128 == 0 and 128 <= c <= 8192, (N, d, V, c)
+            pieces = -(-N // c)
+            assert c - 128 < -(-N // pieces) <= c            # equal chunks
+            assert c == 128 or c * d * elem <= l2, (N, d, V, c)
+            assert c == 128 or c * ldg * elem <= 4 << 30
+        dt_ = int(rng.integers(1, 1024)) * 8
+        cf = lib.kd_full_kl_default_chunk(N, d, dt_, V)
+        assert cf % 128 == 0 and 128 <= cf <= 8192
+        assert cf == 128 or cf * (d + dt_) * 2 <= l2, (N, d, dt_, V, cf)
+        assert cf == 128 or 2 * cf * ldg * 2 <= 8 << 30
 
 
 def call_fwd_bwd(lib, **kw):
