@@ -79,8 +79,9 @@ extern "C" {
 int64_t kd_full_kl_default_chunk(int64_t N, int64_t d_s, int64_t d_t, int64_t V) {
   // Both models' exponential tiles (2 x chunk x V bf16) near 8 GiB; both
   // models' hidden states of the chunk resident in L2 (at 32K tokens,
-  // d_s = d_t = 2880, V = 201,088: chunk 8192 133.5 ms per step, 4096 125.4,
-  // 3072 126.3, 2048 129.5); equal chunks, multiples of 128 rows.
+  // d_s = d_t = 2880, V = 201,088, on one GPU: chunk 8192 133.5 ms per step,
+  // 5504 130.7, 4096 127.3; on another: 4096 125.4, 3072 126.3, 2048 129.5);
+  // equal chunks, multiples of 128 rows.
   const int64_t ldg = kd::round_up(V < 1 ? 1 : V, kd::kBN);
   int64_t cmax = (int64_t(8) << 30) / (4 * ldg);
   cmax = cmax / kd::kBM * kd::kBM;
